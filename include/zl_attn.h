@@ -1,0 +1,210 @@
+/*
+ * zl_attn.h -- C ABI of the coalesced varlen attention library (libzl_attn.so).
+ *
+ * The operation is the attention call of the Coalesced Attention Engine in
+ * Zellige, "Moldable Sequence Placement for Mixed Image-Video DiT Training"
+ * (arXiv 2608.01150v1), §IV-D: all whole sequences of one GPU are packed into
+ * ONE block-diagonal softmax-attention call that keeps the sequences separate
+ * and returns outputs in input order, and shards of split long sequences run
+ * alongside them.  Per sequence s and head h (full bidirectional attention,
+ * §II-A, no mask):
+ *
+ *     S   = Q_s K_s^T * scale
+ *     O_s = softmax(S) V_s            (row-wise softmax)
+ *     LSE = log(sum_j exp(S_ij))      (natural log, one value per query row)
+ *
+ * Conventions shared by every entry point
+ *   - Packed token layout.  Q/O are [Tq, H, d] and K/V are [Tk, H, d],
+ *     row-major, d contiguous.  Sequence s owns query rows
+ *     [cu_seqlens_q[s], cu_seqlens_q[s+1]) and key rows
+ *     [cu_seqlens_k[s], cu_seqlens_k[s+1]).  Tq = cu_seqlens_q[num_seqs].
+ *   - LSE buffers are head-major: lse[h * Tq + row], float32.
+ *   - cu_seqlens_* and tile tables are HOST arrays (int32, num_seqs + 1
+ *     entries, cu[0] = 0, non-decreasing).  All other pointers are DEVICE
+ *     pointers of the current CUDA device, 16-byte aligned.
+ *   - The caller owns every buffer.  The library allocates no device or host
+ *     memory; scratch comes from the caller's `workspace`.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and return after enqueue.  Arguments are validated on the host
+ *     before anything is enqueued; an invalid call returns an error and leaves
+ *     every output untouched.  Device-side faults surface through
+ *     zl_sync_check().
+ *   - Every entry point returns a zl_status (0 = success, < 0 = error) and
+ *     never aborts the process.
+ *   - Thread-safe; the only global state is a per-device cache of device
+ *     attributes and a process-wide launch counter.
+ */
+#ifndef ZL_ATTN_H
+#define ZL_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ZL_OK = 0,
+  ZL_EINVAL = -1,        /* malformed arguments (sizes, cu_seqlens, tile table) */
+  ZL_EUNSUPPORTED = -2,  /* valid but not implemented (head_dim, dtype, mode)   */
+  ZL_EALIGN = -3,        /* a device pointer is not 16-byte aligned             */
+  ZL_EWORKSPACE = -4,    /* workspace missing or smaller than required          */
+  ZL_ECUDA = -5,         /* a CUDA runtime/driver call failed                   */
+  ZL_ETIMEOUT = -6,      /* a kernel gave up a bounded wait (reported by
+                            zl_sync_check)                                      */
+  ZL_ENODEVICE = -7      /* no usable sm_103 device                             */
+} zl_status;
+
+typedef enum {
+  ZL_BF16 = 0,           /* bf16 inputs/outputs, float32 accumulation, tensor cores */
+  ZL_FP32 = 1            /* float32 inputs/outputs, float32 SIMT arithmetic         */
+} zl_dtype;
+
+/*
+ * One (query-chunk x KV-chunk) tile of a split sequence.  Zellige §IV-D runs
+ * shards of split sequences alongside whole ones; §II-B and Table II describe
+ * how a split sequence's attention is computed from K/V blocks and
+ * accumulated exactly.  Offsets are relative to the sequence's own query and
+ * key ranges.
+ *
+ * The tiles of a sequence must form a full grid: n_q_chunks x n_kv_chunks
+ * tiles, one per (q_chunk, kv_chunk), whose query ranges partition the
+ * sequence's queries and whose key ranges partition its keys (every tile with
+ * the same q_chunk has the same query range, every tile with the same kv_chunk
+ * the same key range, chunk ranges contiguous and in chunk order, no empty
+ * chunk).  A sequence listed in the tile table is not also run whole.
+ */
+typedef struct {
+  int32_t seq;          /* index into cu_seqlens_q / cu_seqlens_k             */
+  int32_t q_start;      /* first query of the chunk, relative to the sequence */
+  int32_t q_len;        /* >= 1                                               */
+  int32_t k_start;      /* first key of the chunk, relative to the sequence   */
+  int32_t k_len;        /* >= 1                                               */
+  int32_t q_chunk;      /* 0 .. n_q_chunks-1                                  */
+  int32_t kv_chunk;     /* 0 .. n_kv_chunks-1: the partial slot it writes     */
+  int32_t n_kv_chunks;  /* same for every tile of the sequence, 1 .. 64       */
+} zl_tile_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* zl_status_string(int32_t status);
+
+/* ABI version of this header: (major << 16) | minor. */
+int32_t zl_version(void);
+
+/*
+ * Workspace needed by zl_varlen_attn_fwd for this batch, in bytes (0 when no
+ * sequence is split).  It holds the float32 shard partials: for the split
+ * sequences (in sequence order, R = sum of their query lengths, P = largest
+ * n_kv_chunks) an O partial [P][R][H][d] and an LSE partial [P][H][R].
+ * Same argument rules as zl_varlen_attn_fwd.  Writes the size to *bytes.
+ */
+zl_status zl_varlen_attn_fwd_workspace_size(
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
+    int32_t num_heads, int32_t head_dim, const zl_tile_t* tiles, int32_t num_tiles,
+    size_t* bytes);
+
+/*
+ * Forward of the coalesced block-diagonal attention (Zellige §IV-D).
+ *
+ * q [Tq,H,d], k/v [Tk,H,d]     inputs, dtype `dtype`, device
+ * cu_seqlens_q, cu_seqlens_k   host, num_seqs + 1 entries each
+ * num_heads H >= 1, head_dim d in {64, 128}
+ * softmax_scale                > 0; pass 1/sqrt(d) for the usual scaling
+ * tiles, num_tiles             host tile table (may be NULL when 0)
+ * o [Tq,H,d]                   output, same dtype as the inputs
+ * lse [H,Tq]                   output, float32, natural log
+ * workspace                    device, >= zl_varlen_attn_fwd_workspace_size
+ *
+ * Whole sequences and every tile run in one persistent launch whose work
+ * items (sequence-or-tile x head x 128-query block) are ordered longest
+ * first, ties in input order.  Tiles write float32 partials into the
+ * workspace, and one merge launch (zl_lse_merge's kernel) then combines each
+ * query row's partials into o and lse exactly.  A sequence with queries but no
+ * keys is rejected (ZL_EINVAL); zero-length sequences are skipped.
+ */
+zl_status zl_varlen_attn_fwd(
+    const void* q, const void* k, const void* v,
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
+    int32_t num_heads, int32_t head_dim, int32_t dtype, float softmax_scale,
+    const zl_tile_t* tiles, int32_t num_tiles,
+    void* o, float* lse,
+    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Exact merge of partial attention results over disjoint key sets: the
+ * accumulation step of block-wise (ring / all-gather) attention in Zellige
+ * §II-B and Table II.  For every query row r and head h:
+ *
+ *     lse = log(sum_p exp(lse_p))
+ *     o   = sum_p exp(lse_p - lse) * o_p
+ *
+ * A row whose partials all have lse_p = -inf gets o = 0, lse = -inf.
+ *
+ * o_partial    device float32, part p row r head h at
+ *              ((p * part_stride_rows + r) * H + h) * d
+ * lse_partial  device float32, at (p * H + h) * part_stride_rows + r
+ * n_parts      1 .. 64;  rows >= 0;  part_stride_rows >= rows
+ * o            device, [rows][H][d] in out_dtype (ZL_BF16: round to nearest
+ *              even; ZL_FP32)
+ * lse          device float32, at h * lse_head_stride + r; lse_head_stride
+ *              >= rows
+ * Memory-bound; one launch.
+ */
+zl_status zl_lse_merge(
+    const float* o_partial, const float* lse_partial, int32_t n_parts,
+    int64_t rows, int32_t num_heads, int32_t head_dim, int64_t part_stride_rows,
+    void* o, int32_t out_dtype, float* lse, int64_t lse_head_stride, void* stream);
+
+/*
+ * Workspace needed by zl_varlen_attn_bwd, in bytes: a float32 dQ accumulator
+ * [Tq][H][d] and the float32 row term D = rowsum(dO * O) [H][Tq].
+ */
+zl_status zl_varlen_attn_bwd_workspace_size(
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
+    int32_t num_heads, int32_t head_dim, size_t* bytes);
+
+/*
+ * Backward of zl_varlen_attn_fwd: the analytic gradient of
+ * O = softmax(Q K^T * scale) V per sequence and head (the paper trains with
+ * exact backward, §V-A; the formula is plain calculus):
+ *
+ *     P  = exp(S - LSE)      (recomputed from the forward's LSE)
+ *     D  = rowsum(dO * O)
+ *     dV = P^T dO,   dS = P * (dO V^T - D),
+ *     dQ = scale * dS K,   dK = scale * dS^T Q
+ *
+ * q, k, v, o, dout    device, dtype `dtype` (ZL_BF16 only), layouts as above
+ * lse                 device float32 [H][Tq] from the forward
+ * tiles               the forward's tile table: the backward of a split
+ *                     sequence sums the contributions of all of its tiles,
+ *                     which equals the backward of the whole sequence, so it
+ *                     is computed that way (validated, then run whole)
+ * dq [Tq,H,d], dk/dv [Tk,H,d]   outputs, dtype `dtype`
+ * workspace           device, >= zl_varlen_attn_bwd_workspace_size
+ */
+zl_status zl_varlen_attn_bwd(
+    const void* q, const void* k, const void* v, const void* o, const float* lse,
+    const void* dout,
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
+    int32_t num_heads, int32_t head_dim, int32_t dtype, float softmax_scale,
+    const zl_tile_t* tiles, int32_t num_tiles,
+    void* dq, void* dk, void* dv,
+    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronizes `stream`, then reports (and clears) any error a kernel of this
+ * library flagged on the current device: ZL_ETIMEOUT when a bounded wait
+ * inside a kernel ran out (the kernel stopped early and its outputs are
+ * undefined), ZL_ECUDA for a CUDA error.  ZL_OK otherwise.
+ */
+zl_status zl_sync_check(void* stream);
+
+/* Number of kernel launches this library has enqueued in this process. */
+int64_t zl_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZL_ATTN_H */

@@ -1,0 +1,153 @@
+"""PyTorch-facing wrappers of the C ABI.  torch supplies device memory and the
+current CUDA stream; the arithmetic is entirely in libzl_attn.so.
+
+Tensors: q/o [Tq, H, d], k/v [Tk, H, d] contiguous CUDA tensors (bf16 for the
+tensor-core path, float32 for the float32 path); lse [H, Tq] float32.
+cu_seqlens are host sequences of ints (B+1 entries, starting at 0).
+tiles are tuples (seq, q_start, q_len, k_start, k_len, q_chunk, kv_chunk,
+n_kv_chunks), see zl_tile_t in include/zl_attn.h.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _lib
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return _lib.ZL_BF16
+    if t.dtype == torch.float32:
+        return _lib.ZL_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _check_tensor(t, name):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def fwd_workspace_bytes(cu_seqlens_q, cu_seqlens_k, num_heads, head_dim, tiles=None) -> int:
+    lib = _lib.load()
+    cq, nq = _lib.int32_array(cu_seqlens_q)
+    ck, _ = _lib.int32_array(cu_seqlens_k)
+    ta, nt = _lib.tile_array(tiles)
+    out = ctypes.c_size_t(0)
+    _lib.check(lib.zl_varlen_attn_fwd_workspace_size(cq, ck, nq - 1, num_heads, head_dim, ta, nt,
+                                                     ctypes.byref(out)), "workspace_size")
+    return int(out.value)
+
+
+def bwd_workspace_bytes(cu_seqlens_q, cu_seqlens_k, num_heads, head_dim) -> int:
+    lib = _lib.load()
+    cq, nq = _lib.int32_array(cu_seqlens_q)
+    ck, _ = _lib.int32_array(cu_seqlens_k)
+    out = ctypes.c_size_t(0)
+    _lib.check(lib.zl_varlen_attn_bwd_workspace_size(cq, ck, nq - 1, num_heads, head_dim,
+                                                     ctypes.byref(out)), "bwd_workspace_size")
+    return int(out.value)
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor | None:
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k=None, tiles=None, softmax_scale=None,
+                    out=None, lse=None, workspace=None, stream=None):
+    """Coalesced block-diagonal attention forward.  Returns (o, lse)."""
+    lib = _lib.load()
+    if cu_seqlens_k is None:
+        cu_seqlens_k = cu_seqlens_q
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n)
+    tq, nh, hd = q.shape
+    scale = 1.0 / math.sqrt(hd) if softmax_scale is None else float(softmax_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((nh, tq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(fwd_workspace_bytes(cu_seqlens_q, cu_seqlens_k, nh, hd, tiles), q.device)
+    cq, nq = _lib.int32_array(cu_seqlens_q)
+    ck, nk = _lib.int32_array(cu_seqlens_k)
+    if nq != nk:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k differ in length")
+    ta, nt = _lib.tile_array(tiles)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    st = lib.zl_varlen_attn_fwd(_ptr(q), _ptr(k), _ptr(v), cq, ck, nq - 1, nh, hd, _dtype_code(q),
+                                scale, ta, nt, _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                                _stream_handle(stream))
+    _lib.check(st, "zl_varlen_attn_fwd")
+    return out, lse
+
+
+def varlen_attn_bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k=None, tiles=None,
+                    softmax_scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward of varlen_attn_fwd.  Returns (dq, dk, dv)."""
+    lib = _lib.load()
+    if cu_seqlens_k is None:
+        cu_seqlens_k = cu_seqlens_q
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"), (dout, "dout")):
+        _check_tensor(t, n)
+    tq, nh, hd = q.shape
+    scale = 1.0 / math.sqrt(hd) if softmax_scale is None else float(softmax_scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = alloc_workspace(bwd_workspace_bytes(cu_seqlens_q, cu_seqlens_k, nh, hd), q.device)
+    cq, nq = _lib.int32_array(cu_seqlens_q)
+    ck, _ = _lib.int32_array(cu_seqlens_k)
+    ta, nt = _lib.tile_array(tiles)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    st = lib.zl_varlen_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), cq, ck,
+                                nq - 1, nh, hd, _dtype_code(q), scale, ta, nt, _ptr(dq), _ptr(dk),
+                                _ptr(dv), _ptr(workspace), ws_bytes, _stream_handle(stream))
+    _lib.check(st, "zl_varlen_attn_bwd")
+    return dq, dk, dv
+
+
+def lse_merge(o_partial, lse_partial, rows=None, out_dtype=torch.bfloat16, out=None, lse=None,
+              lse_head_stride=None, stream=None):
+    """Exact merge of partials o_partial [P, R, H, d] / lse_partial [P, H, R]
+    (float32) into (o [rows, H, d], lse [H, rows])."""
+    lib = _lib.load()
+    _check_tensor(o_partial, "o_partial")
+    _check_tensor(lse_partial, "lse_partial")
+    n_parts, part_rows, nh, hd = o_partial.shape
+    rows = part_rows if rows is None else int(rows)
+    if out is None:
+        out = torch.empty((rows, nh, hd), dtype=out_dtype, device=o_partial.device)
+    if lse is None:
+        lse = torch.empty((nh, rows), dtype=torch.float32, device=o_partial.device)
+        lse_head_stride = rows
+    code = _lib.ZL_BF16 if out.dtype == torch.bfloat16 else _lib.ZL_FP32
+    st = lib.zl_lse_merge(_ptr(o_partial), _ptr(lse_partial), n_parts, rows, nh, hd, part_rows,
+                          _ptr(out), code, _ptr(lse), int(lse_head_stride or rows),
+                          _stream_handle(stream))
+    _lib.check(st, "zl_lse_merge")
+    return out, lse
+
+
+def sync_check(stream=None) -> None:
+    """Synchronises the stream and raises if a kernel flagged an error."""
+    _lib.check(_lib.load().zl_sync_check(_stream_handle(stream)), "zl_sync_check")
+
+
+def launch_count() -> int:
+    return int(_lib.load().zl_launch_count())

@@ -1,0 +1,381 @@
+// Forward of coalesced varlen attention on sm_103a tensor cores.
+//
+// One persistent launch runs every work item of the batch: a work item is
+// (segment, head, 128-row query block), where a segment is a whole sequence
+// or one (query-chunk x KV-chunk) shard tile of a split sequence (Zellige,
+// arXiv 2608.01150v1, §IV-D: whole sequences packed into one block-diagonal
+// call, shards alongside them).  Items arrive ordered longest-first from the
+// host scheduler and are taken in a static stride by the CTAs.
+//
+// Per CTA (192 threads, two CTAs per SM):
+//   warp 4     TMA producer: Q tile once per item, then K_j / V_j tiles
+//              through a two-stage ring (128-byte swizzle, 64-column boxes).
+//   warp 5     MMA issuer (one thread):  S = Q K_j^T  (SS, M=128 N=128) into
+//              TMEM, then O += P V_j  (TS: P read from TMEM, V from shared
+//              memory as an MN-major operand) into TMEM.
+//   warps 0-3  softmax: thread t owns query row t = TMEM lane t.  Loads its S
+//              row, tracks the running max m and sum l in base 2, writes
+//              P = 2^(S*scale*log2e - m) as bf16 over the S columns, and
+//              rescales the O row in TMEM when m grows by more than 2^8
+//              (lazy rescale; exactness holds for any m used consistently).
+//              After the last block it normalises O and writes O and LSE.
+// TMEM: S/P in columns [0,128), O in [128, 128+d); 256 columns per CTA.
+//
+// Whole sequences write O in bf16 and LSE in natural log; tiles write float32
+// partial O and their own LSE into a partial slot for the merge kernel.
+#include "common.cuh"
+#include "launch.h"
+#include "work.cuh"
+
+namespace zl {
+namespace {
+
+__device__ uint32_t g_fwd_err;
+
+constexpr int kFwdThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kFwdStages = 2;
+constexpr uint32_t kTmemCols = 256;
+constexpr float kRescaleThreshold = 8.0f;   // in log2 units: P <= 2^8
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int HD>
+struct FwdSmem {
+  uint8_t q[kBlockM * HD * 2];                 // HD/64 boxes of [128 rows][128 B]
+  uint8_t kv[kFwdStages][kBlockN * HD * 2];    // K_j or V_j, same box layout
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[kFwdStages], kv_empty[kFwdStages];
+  uint64_t s_full, p_full, o_full;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Spin for about `ns` nanoseconds: lets copies and MMAs already in flight land
+// before an aborting CTA releases its shared memory and TMEM.
+__device__ __forceinline__ void drain_delay(uint64_t ns) {
+  const uint64_t t0 = globaltimer();
+  while (globaltimer() - t0 < ns) {
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kFwdThreads, 2)
+fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdArgs args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  auto* sm = reinterpret_cast<FwdSmem<HD>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort_flag = &sm->abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm->q_full, 1);
+    mbar_init(&sm->q_empty, 1);
+    for (int s = 0; s < kFwdStages; ++s) {
+      mbar_init(&sm->kv_full[s], 1);
+      mbar_init(&sm->kv_empty[s], 1);
+    }
+    mbar_init(&sm->s_full, 1);
+    mbar_init(&sm->p_full, 128);
+    mbar_init(&sm->o_full, 1);
+    sm->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&sm->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  const uint32_t tS = tmem;          // S (f32) / P (bf16 pairs) columns [0,128)
+  const uint32_t tO = tmem + 128;    // O (f32) columns [128, 128+HD)
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      uint32_t kv_it = 0, item_it = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x, ++item_it) {
+        const FwdWork w = decode_fwd(args, it);
+        const FwdSeg& sg = args.segs[w.seg];
+        const int q_row = sg.q_row0 + w.qb * kBlockM;
+        const int nkb = (sg.k_len + kBlockN - 1) / kBlockN;
+        const int x0 = w.h * HD;
+        if (!mbar_wait(&sm->q_empty, (item_it & 1u) ^ 1u, abort_flag, &g_fwd_err,
+                       ERR_TIMEOUT_PRODUCER)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&sm->q_full, kBlockM * HD * 2);
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c)
+          tma_load_2d(sm->q + c * kBlockM * 128, &tmQ, &sm->q_full, x0 + c * 64, q_row);
+        for (int j = 0; j < nkb && ok; ++j) {
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {
+            const uint32_t st = kv_it % kFwdStages;
+            const uint32_t ph = (kv_it / kFwdStages) & 1u;
+            if (!mbar_wait(&sm->kv_empty[st], ph ^ 1u, abort_flag, &g_fwd_err,
+                           ERR_TIMEOUT_PRODUCER)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sm->kv_full[st], kBlockN * HD * 2);
+            const CUtensorMap* map = kv ? &tmV : &tmK;
+#pragma unroll
+            for (int c = 0; c < HD / 64; ++c)
+              tma_load_2d(sm->kv[st] + c * kBlockN * 128, map, &sm->kv_full[st], x0 + c * 64,
+                          sg.k_row0 + j * kBlockN);
+            ++kv_it;
+          }
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16(kBlockM, kBlockN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(kBlockM, HD, false, true);
+      const uint32_t q_addr = smem_u32(sm->q);
+      uint32_t kv_it = 0, item_it = 0, blk_it = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x, ++item_it) {
+        const FwdWork w = decode_fwd(args, it);
+        const FwdSeg& sg = args.segs[w.seg];
+        const int nkb = (sg.k_len + kBlockN - 1) / kBlockN;
+        if (!mbar_wait(&sm->q_full, item_it & 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_MMA)) {
+          ok = false;
+          break;
+        }
+        for (int j = 0; j < nkb; ++j, ++blk_it) {
+          // S = Q K_j^T
+          uint32_t st = kv_it % kFwdStages;
+          uint32_t ph = (kv_it / kFwdStages) & 1u;
+          if (!mbar_wait(&sm->kv_full[st], ph, abort_flag, &g_fwd_err, ERR_TIMEOUT_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(sm->kv[st]);
+#pragma unroll
+          for (int ks = 0; ks < HD / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * (kBlockM * 128) + (ks & 3) * 32;
+            umma_ss(tS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+                    idesc_qk, ks > 0 ? 1u : 0u);
+          }
+          umma_commit(&sm->s_full);
+          umma_commit(&sm->kv_empty[st]);
+          if (j == nkb - 1) umma_commit(&sm->q_empty);
+          ++kv_it;
+          // O += P V_j once the softmax warps have written P_j (and rescaled O)
+          st = kv_it % kFwdStages;
+          ph = (kv_it / kFwdStages) & 1u;
+          if (!mbar_wait(&sm->kv_full[st], ph, abort_flag, &g_fwd_err, ERR_TIMEOUT_MMA) ||
+              !mbar_wait(&sm->p_full, blk_it & 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_MMA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t v_addr = smem_u32(sm->kv[st]);
+#pragma unroll
+          for (int ks = 0; ks < kBlockN / 16; ++ks) {
+            umma_ts(tO, tS + ks * 8, sdesc_sw128(v_addr + ks * 2048, kBlockN * 128, 1024),
+                    idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(&sm->kv_empty[st]);
+          ++kv_it;
+        }
+        if (!ok) break;
+        umma_commit(&sm->o_full);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int row = warp * 32 + lane;
+    const float sl2 = args.scale_log2;
+    const int nh = args.num_heads;
+    uint32_t item_it = 0, blk_it = 0;
+    for (int it = blockIdx.x; it < args.n_items; it += gridDim.x, ++item_it) {
+      const FwdWork w = decode_fwd(args, it);
+      const FwdSeg& sg = args.segs[w.seg];
+      const int nkb = (sg.k_len + kBlockN - 1) / kBlockN;
+      float m_run = -INFINITY;
+      float l_run = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nkb; ++j, ++blk_it) {
+        // all lanes must agree before the warp-wide tcgen05.ld below
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&sm->s_full, blk_it & 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_SOFTMAX))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t s[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, s[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) reg_fence(s[c]);
+        const int valid = sg.k_len - j * kBlockN;
+        if (valid < kBlockN) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i >= valid) s[c][i] = __float_as_uint(-INFINITY);
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          mx0 = fmaxf(mx0, __uint_as_float(s[0][i]));
+          mx1 = fmaxf(mx1, __uint_as_float(s[1][i]));
+          mx2 = fmaxf(mx2, __uint_as_float(s[2][i]));
+          mx3 = fmaxf(mx3, __uint_as_float(s[3][i]));
+        }
+        const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const float m_new = fmaxf(m_run, m_blk);
+        const bool need = m_new > m_run + kRescaleThreshold;
+        float alpha = 1.f;
+        if (need) {
+          alpha = fast_exp2(m_run - m_new);   // 0 on the first block (m_run = -inf)
+          m_run = m_new;
+        }
+        l_run *= alpha;
+        const float neg_m = -m_run;
+        float ls0 = 0.f, ls1 = 0.f;
+        uint32_t p[2][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a = fast_exp2(fmaf(__uint_as_float(s[c][2 * i]), sl2, neg_m));
+            const float b = fast_exp2(fmaf(__uint_as_float(s[c][2 * i + 1]), sl2, neg_m));
+            ls0 += a;
+            ls1 += b;
+            p[c >> 1][(c & 1) * 16 + i] = pack_bf16x2(a, b);
+          }
+        }
+        tmem_st32(tS + lane_off + 0, p[0]);
+        tmem_st32(tS + lane_off + 32, p[1]);
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + lane_off + c * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + lane_off + c * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&sm->p_full);
+        l_run += ls0 + ls1;
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&sm->o_full, item_it & 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_SOFTMAX)))
+        break;
+      tc_fence_after();
+      const int q_local = w.qb * kBlockM + row;
+      const bool row_ok = q_local < sg.q_len;
+      const float inv_l = 1.f / l_run;
+      const float lse_val = (m_run + log2f(l_run)) * kLn2;
+      if (sg.slot < 0) {
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.o) +
+                             (static_cast<size_t>(sg.q_row0 + q_local) * nh + w.h) * HD;
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + lane_off + c * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          if (row_ok) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 pk;
+              pk.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+              pk.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+              pk.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+              pk.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+              d4[v] = pk;
+            }
+          }
+        }
+        if (row_ok) args.lse[static_cast<size_t>(w.h) * args.lse_stride + sg.q_row0 + q_local] = lse_val;
+      } else {
+        const size_t prow = static_cast<size_t>(sg.slot) * args.part_rows + sg.out_row0 + q_local;
+        float* dst = args.o_part + (prow * nh + w.h) * HD;
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + lane_off + c * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          if (row_ok) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              d4[v] = make_float4(__uint_as_float(o[4 * v + 0]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                  __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+          }
+        }
+        if (row_ok)
+          args.lse_part[(static_cast<size_t>(sg.slot) * nh + w.h) * args.part_rows + sg.out_row0 + q_local] =
+              lse_val;
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  __syncwarp();
+  if (*abort_flag) drain_delay(2000000ull);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int HD>
+cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const FwdArgs& args, int grid, cudaStream_t stream) {
+  const size_t smem = sizeof(FwdSmem<HD>) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  fwd_tc_kernel<HD><<<grid, kFwdThreads, smem, stream>>>(tq, tk, tv, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t fwd_tc_smem_bytes(int head_dim) {
+  return head_dim == 64 ? sizeof(FwdSmem<64>) + 1024 : sizeof(FwdSmem<128>) + 1024;
+}
+
+cudaError_t launch_fwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const FwdArgs& args, int grid,
+                          cudaStream_t stream) {
+  if (head_dim == 64) return launch_tc<64>(tq, tk, tv, args, grid, stream);
+  if (head_dim == 128) return launch_tc<128>(tq, tk, tv, args, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+uint32_t fwd_take_error() {
+  uint32_t v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fwd_err, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+  if (v != 0) cudaMemcpyToSymbol(g_fwd_err, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace zl

@@ -1,0 +1,110 @@
+// Internal interface between the host library (zl_host.cpp) and the kernel
+// translation units.  Not part of the public C ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace zl {
+
+// Query rows per work item and keys per inner block of the tensor-core
+// kernels.  One 128-row query block maps onto the 128 TMEM lanes.
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+
+// Work segments passed by value in one launch (kernel parameter space).
+constexpr int kMaxSegs = 960;
+
+// One segment of forward work: a whole sequence or one shard tile.  Its work
+// items are (head, 128-row query block) pairs, numbered from item0 with the
+// query block fastest.
+struct FwdSeg {
+  int32_t q_row0;    // packed row of the segment's first query
+  int32_t k_row0;    // packed row of the segment's first key
+  int32_t q_len;     // >= 1
+  int32_t k_len;     // >= 1
+  int32_t out_row0;  // whole: = q_row0 (row in o/lse); tile: row in the partial slot
+  int32_t slot;      // -1: whole sequence, else the partial slot (kv chunk)
+  int32_t item0;     // first work item of the segment
+};
+
+struct FwdArgs {
+  void* o;              // whole-sequence output [Tq][H][d] (bf16 or f32)
+  float* lse;           // [H][lse_stride]
+  float* o_part;        // partial O  [P][part_rows][H][d] f32
+  float* lse_part;      // partial LSE [P][H][part_rows] f32
+  int64_t lse_stride;   // Tq
+  int64_t part_rows;    // R
+  int32_t num_heads;
+  float scale;          // softmax scale
+  float scale_log2;     // scale * log2(e)
+  int32_t n_items;
+  int32_t n_segs;
+  FwdSeg segs[kMaxSegs];
+};
+
+struct MergeArgs {
+  const float* o_part;
+  const float* lse_part;
+  void* o;
+  float* lse;
+  int64_t rows;
+  int64_t part_stride_rows;
+  int64_t lse_head_stride;
+  int32_t n_parts;
+  int32_t num_heads;
+  int32_t out_bf16;
+};
+
+// Backward work: one item per (sequence, head, 128-key block); the item loops
+// over every 128-row query block of the sequence.
+struct BwdSeg {
+  int32_t q_row0;
+  int32_t k_row0;
+  int32_t q_len;
+  int32_t k_len;
+  int32_t item0;
+};
+
+struct BwdArgs {
+  const float* lse;      // [H][Tq]
+  const float* dsum;     // D [H][Tq]
+  float* dq_acc;         // [Tq][H][d] f32, zeroed before the launch
+  void* dk;              // [Tk][H][d] bf16
+  void* dv;              // [Tk][H][d] bf16
+  int64_t lse_stride;    // Tq
+  int32_t num_heads;
+  float scale;
+  float scale_log2;
+  int32_t n_items;
+  int32_t n_segs;
+  BwdSeg segs[kMaxSegs];
+};
+
+// ---------------------------------------------------------------- launchers
+// Each returns the CUDA error of the launch (cudaSuccess when enqueued).
+cudaError_t launch_fwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const FwdArgs& args, int grid,
+                          cudaStream_t stream);
+cudaError_t launch_fwd_f32(int head_dim, const float* q, const float* k, const float* v,
+                           const FwdArgs& args, cudaStream_t stream);
+cudaError_t launch_merge(int head_dim, const MergeArgs& args, int num_sms, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(int head_dim, const void* o, const void* dout, float* dsum,
+                                  int64_t tq, int32_t num_heads, int num_sms,
+                                  cudaStream_t stream);
+cudaError_t launch_bwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
+                          int grid, cudaStream_t stream);
+cudaError_t launch_dq_convert(int head_dim, const float* dq_acc, void* dq, int64_t tq,
+                              int32_t num_heads, float scale, int num_sms, cudaStream_t stream);
+
+// Shared-memory bytes a CTA of the tensor-core forward / backward requests.
+size_t fwd_tc_smem_bytes(int head_dim);
+size_t bwd_tc_smem_bytes(int head_dim);
+
+// Error words recorded by bounded waits in each kernel family (read and
+// cleared; synchronous).
+uint32_t fwd_take_error();
+uint32_t bwd_take_error();
+
+}  // namespace zl

@@ -1,0 +1,473 @@
+// Host side of libzl_attn: argument validation, the longest-first tile
+// scheduler, workspace layout, tensor-map setup and kernel launches behind
+// the C ABI in include/zl_attn.h.
+//
+// Scheduling (Zellige, arXiv 2608.01150v1, §IV-D): the engine runs whole
+// sequences and the shards of split sequences together and orders its
+// segments stably, ties broken by placement order; the planner's filler stage
+// (§IV-C, Eq. 8 and Alg. 1) takes sequences in decreasing price.  On one GPU
+// the same largest-first idea becomes: every segment (whole sequence or tile)
+// is costed by the keys each of its 128-row query blocks must visit, segments
+// are stably sorted by decreasing cost (ties keep input order), and the
+// persistent grid takes work items in that order so the long video blocks
+// start first and the cheap image blocks fill the tail.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "zl_attn.h"
+
+namespace {
+
+using zl::FwdArgs;
+using zl::FwdSeg;
+using zl::kBlockM;
+using zl::kBlockN;
+using zl::kMaxSegs;
+
+std::atomic<int64_t> g_launches{0};
+
+// ------------------------------------------------------------------ device
+struct DevInfo {
+  int sms = 0;
+  int status = 1;  // 1 = not queried yet, else a zl_status
+};
+std::mutex g_dev_mu;
+DevInfo g_dev[128];
+
+zl_status device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ZL_ENODEVICE;
+  }
+  if (dev < 0 || dev >= 128) return ZL_ENODEVICE;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (d.status == 1) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      d.status = ZL_ECUDA;
+    } else if (major != 10 || minor != 3) {
+      d.status = ZL_ENODEVICE;   // the kernels are built for sm_103a only
+    } else {
+      d.sms = n;
+      d.status = ZL_OK;
+    }
+  }
+  *sms = d.sms;
+  return static_cast<zl_status>(d.status);
+}
+
+// ------------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// 2D view [rows][H*d] of a packed bf16 tensor; boxes of 64 columns x 128 rows
+// with the 128-byte swizzle the UMMA descriptors expect.  Rows past the end
+// read as zero.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int nh, int hd) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nh) * hd, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nh) * hd * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ validation
+struct SplitSeq {
+  int seq = 0;
+  int n_kv = 0;
+  int64_t rbase = 0;   // first row of this sequence in every partial slot
+  int64_t len = 0;     // query length
+};
+
+struct Plan {
+  int64_t tq = 0, tk = 0;
+  std::vector<int> split_index;     // per sequence: -1, or index into splits
+  std::vector<SplitSeq> splits;
+  std::vector<zl_tile_t> tiles;     // sorted by (seq, q_chunk, kv_chunk)
+  int64_t part_rows = 0;            // R
+  int n_parts = 0;                  // P
+};
+
+constexpr int64_t kMaxTokens = (int64_t(1) << 31) - 1 - 2 * kBlockM;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+zl_status check_cu(const int32_t* cu, int32_t b, int64_t* total) {
+  if (!cu) return ZL_EINVAL;
+  if (cu[0] != 0) return ZL_EINVAL;
+  for (int32_t s = 0; s < b; ++s)
+    if (cu[s + 1] < cu[s]) return ZL_EINVAL;
+  *total = cu[b];
+  if (*total > kMaxTokens) return ZL_EINVAL;
+  return ZL_OK;
+}
+
+zl_status make_plan(const int32_t* cu_q, const int32_t* cu_k, int32_t b, int32_t nh, int32_t hd,
+                    const zl_tile_t* tiles, int32_t n_tiles, Plan* plan) {
+  if (b < 0 || n_tiles < 0 || nh < 1 || nh > 4096) return ZL_EINVAL;
+  if (hd != 64 && hd != 128) return ZL_EUNSUPPORTED;
+  zl_status st = check_cu(cu_q, b, &plan->tq);
+  if (st != ZL_OK) return st;
+  st = check_cu(cu_k, b, &plan->tk);
+  if (st != ZL_OK) return st;
+  if ((plan->tq + kBlockM) * int64_t(nh) * hd > (int64_t(1) << 40)) return ZL_EINVAL;
+  for (int32_t s = 0; s < b; ++s)
+    if (cu_q[s + 1] > cu_q[s] && cu_k[s + 1] == cu_k[s]) return ZL_EINVAL;  // queries without keys
+  plan->split_index.assign(static_cast<size_t>(b), -1);
+  plan->splits.clear();
+  plan->tiles.clear();
+  if (n_tiles == 0) return ZL_OK;
+  if (!tiles) return ZL_EINVAL;
+  plan->tiles.assign(tiles, tiles + n_tiles);
+  for (const zl_tile_t& t : plan->tiles) {
+    if (t.seq < 0 || t.seq >= b) return ZL_EINVAL;
+    const int64_t lq = cu_q[t.seq + 1] - cu_q[t.seq];
+    const int64_t lk = cu_k[t.seq + 1] - cu_k[t.seq];
+    if (t.n_kv_chunks < 1 || t.n_kv_chunks > 64) return ZL_EINVAL;
+    if (t.kv_chunk < 0 || t.kv_chunk >= t.n_kv_chunks || t.q_chunk < 0 || t.q_chunk >= 1 << 20)
+      return ZL_EINVAL;
+    if (t.q_len < 1 || t.k_len < 1 || t.q_start < 0 || t.k_start < 0) return ZL_EINVAL;
+    if (int64_t(t.q_start) + t.q_len > lq || int64_t(t.k_start) + t.k_len > lk) return ZL_EINVAL;
+  }
+  std::stable_sort(plan->tiles.begin(), plan->tiles.end(), [](const zl_tile_t& a, const zl_tile_t& c) {
+    if (a.seq != c.seq) return a.seq < c.seq;
+    if (a.q_chunk != c.q_chunk) return a.q_chunk < c.q_chunk;
+    return a.kv_chunk < c.kv_chunk;
+  });
+  // Each split sequence: a full n_q x n_kv grid of tiles partitioning its
+  // query range and its key range into contiguous chunks in chunk order.
+  size_t i = 0;
+  int64_t rbase = 0;
+  while (i < plan->tiles.size()) {
+    const int seq = plan->tiles[i].seq;
+    size_t j = i;
+    while (j < plan->tiles.size() && plan->tiles[j].seq == seq) ++j;
+    const int n_kv = plan->tiles[i].n_kv_chunks;
+    const size_t cnt = j - i;
+    if (cnt % static_cast<size_t>(n_kv) != 0) return ZL_EINVAL;
+    const int n_q = static_cast<int>(cnt / static_cast<size_t>(n_kv));
+    const int64_t lq = cu_q[seq + 1] - cu_q[seq];
+    const int64_t lk = cu_k[seq + 1] - cu_k[seq];
+    int64_t q_expect = 0;
+    for (int qc = 0; qc < n_q; ++qc) {
+      int64_t k_expect = 0;
+      const zl_tile_t& first = plan->tiles[i + static_cast<size_t>(qc) * n_kv];
+      if (first.q_start != q_expect) return ZL_EINVAL;
+      for (int kc = 0; kc < n_kv; ++kc) {
+        const zl_tile_t& t = plan->tiles[i + static_cast<size_t>(qc) * n_kv + kc];
+        if (t.n_kv_chunks != n_kv || t.q_chunk != qc || t.kv_chunk != kc) return ZL_EINVAL;
+        if (t.q_start != first.q_start || t.q_len != first.q_len) return ZL_EINVAL;
+        const zl_tile_t& col0 = plan->tiles[i + kc];   // same kv chunk, q chunk 0
+        if (t.k_start != col0.k_start || t.k_len != col0.k_len) return ZL_EINVAL;
+        if (t.k_start != k_expect) return ZL_EINVAL;
+        k_expect += t.k_len;
+      }
+      if (k_expect != lk) return ZL_EINVAL;
+      q_expect += first.q_len;
+    }
+    if (q_expect != lq) return ZL_EINVAL;
+    SplitSeq sp;
+    sp.seq = seq;
+    sp.n_kv = n_kv;
+    sp.rbase = rbase;
+    sp.len = lq;
+    plan->split_index[static_cast<size_t>(seq)] = static_cast<int>(plan->splits.size());
+    plan->splits.push_back(sp);
+    rbase += lq;
+    plan->n_parts = std::max(plan->n_parts, n_kv);
+    i = j;
+  }
+  plan->part_rows = rbase;
+  return ZL_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t fwd_workspace_bytes(const Plan& p, int nh, int hd) {
+  if (p.splits.empty()) return 0;
+  const size_t o_bytes = static_cast<size_t>(p.n_parts) * p.part_rows * nh * hd * sizeof(float);
+  const size_t l_bytes = static_cast<size_t>(p.n_parts) * nh * p.part_rows * sizeof(float);
+  return align256(o_bytes) + align256(l_bytes);
+}
+
+// ------------------------------------------------------------------ scheduler
+struct Segment {
+  FwdSeg seg;
+  int64_t cost;   // keys visited per query block
+  int order;      // input order (sequence index, then tile order)
+};
+
+// Whole sequences and tiles as segments, stably ordered by decreasing cost.
+std::vector<Segment> schedule_fwd(const Plan& p, const int32_t* cu_q, const int32_t* cu_k, int32_t b) {
+  std::vector<Segment> segs;
+  segs.reserve(static_cast<size_t>(b) + p.tiles.size());
+  size_t ti = 0;
+  int order = 0;
+  for (int32_t s = 0; s < b; ++s) {
+    const int32_t lq = cu_q[s + 1] - cu_q[s];
+    const int32_t lk = cu_k[s + 1] - cu_k[s];
+    const int si = p.split_index[static_cast<size_t>(s)];
+    if (si < 0) {
+      if (lq == 0) continue;
+      Segment g;
+      g.seg = FwdSeg{cu_q[s], cu_k[s], lq, lk, cu_q[s], -1, 0};
+      g.cost = lk;
+      g.order = order++;
+      segs.push_back(g);
+    } else {
+      const SplitSeq& sp = p.splits[static_cast<size_t>(si)];
+      while (ti < p.tiles.size() && p.tiles[ti].seq < s) ++ti;
+      for (; ti < p.tiles.size() && p.tiles[ti].seq == s; ++ti) {
+        const zl_tile_t& t = p.tiles[ti];
+        Segment g;
+        g.seg = FwdSeg{cu_q[s] + t.q_start, cu_k[s] + t.k_start, t.q_len, t.k_len,
+                       static_cast<int32_t>(sp.rbase + t.q_start), t.kv_chunk, 0};
+        g.cost = t.k_len;
+        g.order = order++;
+        segs.push_back(g);
+      }
+    }
+  }
+  std::stable_sort(segs.begin(), segs.end(),
+                   [](const Segment& a, const Segment& c) { return a.cost > c.cost; });
+  return segs;
+}
+
+// Fills args.segs with segments [first, last) and numbers their items.
+void fill_args(FwdArgs* args, const std::vector<Segment>& segs, size_t first, size_t last, int nh) {
+  int64_t items = 0;
+  args->n_segs = static_cast<int32_t>(last - first);
+  for (size_t i = first; i < last; ++i) {
+    FwdSeg s = segs[i].seg;
+    s.item0 = static_cast<int32_t>(items);
+    args->segs[i - first] = s;
+    items += int64_t(nh) * ((s.q_len + kBlockM - 1) / kBlockM);
+  }
+  args->n_items = static_cast<int32_t>(items);
+}
+
+zl_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return ZL_OK;
+  cudaGetLastError();
+  return ZL_ECUDA;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+extern "C" {
+
+const char* zl_status_string(int32_t status) {
+  switch (status) {
+    case ZL_OK: return "ok";
+    case ZL_EINVAL: return "invalid argument";
+    case ZL_EUNSUPPORTED: return "unsupported configuration";
+    case ZL_EALIGN: return "device pointer not 16-byte aligned";
+    case ZL_EWORKSPACE: return "workspace missing or too small";
+    case ZL_ECUDA: return "CUDA error";
+    case ZL_ETIMEOUT: return "a kernel gave up a bounded wait";
+    case ZL_ENODEVICE: return "no sm_103 CUDA device";
+    default: return "unknown status";
+  }
+}
+
+int32_t zl_version(void) { return (1 << 16) | 0; }
+
+int64_t zl_launch_count(void) { return g_launches.load(); }
+
+zl_status zl_varlen_attn_fwd_workspace_size(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                            int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                            const zl_tile_t* tiles, int32_t num_tiles, size_t* bytes) {
+  if (!bytes) return ZL_EINVAL;
+  Plan plan;
+  const zl_status st = make_plan(cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, tiles,
+                                 num_tiles, &plan);
+  if (st != ZL_OK) return st;
+  *bytes = fwd_workspace_bytes(plan, num_heads, head_dim);
+  return ZL_OK;
+}
+
+zl_status zl_lse_merge(const float* o_partial, const float* lse_partial, int32_t n_parts, int64_t rows,
+                       int32_t num_heads, int32_t head_dim, int64_t part_stride_rows, void* o,
+                       int32_t out_dtype, float* lse, int64_t lse_head_stride, void* stream) {
+  if (n_parts < 1 || n_parts > 64 || rows < 0 || num_heads < 1 || part_stride_rows < rows ||
+      lse_head_stride < rows)
+    return ZL_EINVAL;
+  if (head_dim != 64 && head_dim != 128) return ZL_EUNSUPPORTED;
+  if (out_dtype != ZL_BF16 && out_dtype != ZL_FP32) return ZL_EUNSUPPORTED;
+  if (rows == 0) return ZL_OK;
+  if (!o_partial || !lse_partial || !o || !lse) return ZL_EINVAL;
+  if (!aligned16(o_partial) || !aligned16(o)) return ZL_EALIGN;
+  if (rows * num_heads > (int64_t(1) << 40)) return ZL_EINVAL;
+  int sms = 0;
+  zl_status st = device_sms(&sms);
+  if (st != ZL_OK) return st;
+  zl::MergeArgs a;
+  a.o_part = o_partial;
+  a.lse_part = lse_partial;
+  a.o = o;
+  a.lse = lse;
+  a.rows = rows;
+  a.part_stride_rows = part_stride_rows;
+  a.lse_head_stride = lse_head_stride;
+  a.n_parts = n_parts;
+  a.num_heads = num_heads;
+  a.out_bf16 = out_dtype == ZL_BF16 ? 1 : 0;
+  st = cuda_status(zl::launch_merge(head_dim, a, sms, static_cast<cudaStream_t>(stream)));
+  if (st == ZL_OK) g_launches.fetch_add(1);
+  return st;
+}
+
+zl_status zl_varlen_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                             const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t num_heads,
+                             int32_t head_dim, int32_t dtype, float softmax_scale, const zl_tile_t* tiles,
+                             int32_t num_tiles, void* o, float* lse, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (dtype != ZL_BF16 && dtype != ZL_FP32) return ZL_EUNSUPPORTED;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return ZL_EINVAL;
+  Plan plan;
+  zl_status st = make_plan(cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, tiles, num_tiles, &plan);
+  if (st != ZL_OK) return st;
+  if (plan.tq == 0) return ZL_OK;
+  if (!q || !k || !v || !o || !lse) return ZL_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ZL_EALIGN;
+  const size_t need = fwd_workspace_bytes(plan, num_heads, head_dim);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return ZL_EWORKSPACE;
+  if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ZL_EALIGN;
+  int sms = 0;
+  st = device_sms(&sms);
+  if (st != ZL_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  const std::vector<Segment> segs = schedule_fwd(plan, cu_seqlens_q, cu_seqlens_k, num_seqs);
+  static thread_local FwdArgs args;   // ~27 KB: kept off the stack
+  std::memset(&args, 0, sizeof(args));
+  args.o = o;
+  args.lse = lse;
+  args.lse_stride = plan.tq;
+  args.num_heads = num_heads;
+  args.scale = softmax_scale;
+  args.scale_log2 = softmax_scale * 1.4426950408889634f;
+  if (need > 0) {
+    char* ws = static_cast<char*>(workspace);
+    args.o_part = reinterpret_cast<float*>(ws);
+    args.lse_part = reinterpret_cast<float*>(
+        ws + align256(static_cast<size_t>(plan.n_parts) * plan.part_rows * num_heads * head_dim * sizeof(float)));
+    args.part_rows = plan.part_rows;
+  }
+  CUtensorMap mq, mk, mv;
+  if (dtype == ZL_BF16) {
+    if (!make_map(&mq, q, plan.tq, num_heads, head_dim) || !make_map(&mk, k, plan.tk, num_heads, head_dim) ||
+        !make_map(&mv, v, plan.tk, num_heads, head_dim))
+      return ZL_ECUDA;
+  }
+  for (size_t first = 0; first < segs.size(); first += kMaxSegs) {
+    const size_t last = std::min(segs.size(), first + kMaxSegs);
+    fill_args(&args, segs, first, last, num_heads);
+    if (args.n_items == 0) continue;
+    cudaError_t e;
+    if (dtype == ZL_BF16) {
+      const int grid = std::min(args.n_items, 2 * sms);
+      e = zl::launch_fwd_tc(head_dim, mq, mk, mv, args, grid, s);
+    } else {
+      e = zl::launch_fwd_f32(head_dim, static_cast<const float*>(q), static_cast<const float*>(k),
+                             static_cast<const float*>(v), args, s);
+    }
+    st = cuda_status(e);
+    if (st != ZL_OK) return st;
+    g_launches.fetch_add(1);
+  }
+  // Combine each split sequence's partial slots into its rows of o and lse.
+  const size_t esz = dtype == ZL_BF16 ? 2 : 4;
+  for (const SplitSeq& sp : plan.splits) {
+    zl::MergeArgs m;
+    m.o_part = args.o_part + static_cast<size_t>(sp.rbase) * num_heads * head_dim;
+    m.lse_part = args.lse_part + sp.rbase;
+    m.o = static_cast<char*>(o) + static_cast<size_t>(cu_seqlens_q[sp.seq]) * num_heads * head_dim * esz;
+    m.lse = lse + cu_seqlens_q[sp.seq];
+    m.rows = sp.len;
+    m.part_stride_rows = plan.part_rows;
+    m.lse_head_stride = plan.tq;
+    m.n_parts = sp.n_kv;
+    m.num_heads = num_heads;
+    m.out_bf16 = dtype == ZL_BF16 ? 1 : 0;
+    st = cuda_status(zl::launch_merge(head_dim, m, sms, s));
+    if (st != ZL_OK) return st;
+    g_launches.fetch_add(1);
+  }
+  return ZL_OK;
+}
+
+zl_status zl_varlen_attn_bwd_workspace_size(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                            int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                            size_t* bytes) {
+  if (!bytes) return ZL_EINVAL;
+  Plan plan;
+  const zl_status st = make_plan(cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, nullptr, 0, &plan);
+  if (st != ZL_OK) return st;
+  *bytes = align256(static_cast<size_t>(plan.tq) * num_heads * head_dim * sizeof(float)) +
+           align256(static_cast<size_t>(plan.tq) * num_heads * sizeof(float));
+  return ZL_OK;
+}
+
+zl_status zl_varlen_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                             const void* dout, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                             int32_t num_seqs, int32_t num_heads, int32_t head_dim, int32_t dtype,
+                             float softmax_scale, const zl_tile_t* tiles, int32_t num_tiles, void* dq,
+                             void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  (void)q; (void)k; (void)v; (void)o; (void)lse; (void)dout; (void)dq; (void)dk; (void)dv;
+  (void)workspace; (void)workspace_bytes; (void)stream;
+  if (dtype != ZL_BF16) return ZL_EUNSUPPORTED;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return ZL_EINVAL;
+  Plan plan;
+  const zl_status st = make_plan(cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, tiles, num_tiles, &plan);
+  if (st != ZL_OK) return st;
+  return ZL_EUNSUPPORTED;
+}
+
+zl_status zl_sync_check(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return ZL_ECUDA;
+  }
+  const uint32_t e = zl::fwd_take_error();
+  if (e == 0xFFFFFFFFu) return ZL_ECUDA;
+  if (e != 0) return ZL_ETIMEOUT;
+  return ZL_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,146 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects malformed calls on the host before any CUDA work
+(Zellige arXiv 2608.01150v1 §IV-C: a plan either succeeds or fails as a
+whole; here an invalid call returns an error and touches no output)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixed_length_dit_gb300 import _lib
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "zl_attn.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(zl_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_lib.EXPORTS)
+
+
+def test_version_and_strings(lib):
+    assert lib.zl_version() >> 16 == 1
+    for code in range(0, -8, -1):
+        assert _lib.status_string(code) not in ("", "unknown status")
+    assert _lib.status_string(-99) == "unknown status"
+
+
+def _fwd(lib, cu_q, cu_k, nh=2, hd=64, tiles=None, dtype=_lib.ZL_BF16, scale=0.125,
+         ptr=64, ws=None, ws_bytes=0):
+    cq, nq = _lib.int32_array(cu_q)
+    ck, _ = _lib.int32_array(cu_k)
+    ta, nt = _lib.tile_array(tiles)
+    p = ctypes.c_void_p(ptr)
+    return lib.zl_varlen_attn_fwd(p, p, p, cq, ck, nq - 1, nh, hd, dtype, scale, ta, nt, p, p,
+                                  ctypes.c_void_p(ws), ws_bytes, None)
+
+
+def test_rejects_bad_cu_seqlens(lib):
+    assert _fwd(lib, [1, 5], [0, 5]) == _lib.ZL_EINVAL          # does not start at 0
+    assert _fwd(lib, [0, 5, 3], [0, 5, 3]) == _lib.ZL_EINVAL    # decreasing
+    assert _fwd(lib, [0, 4], [0, 0]) == _lib.ZL_EINVAL          # queries without keys
+
+
+def test_rejects_bad_shapes_and_types(lib):
+    assert _fwd(lib, [0, 5], [0, 5], hd=96) == _lib.ZL_EUNSUPPORTED
+    assert _fwd(lib, [0, 5], [0, 5], nh=0) == _lib.ZL_EINVAL
+    assert _fwd(lib, [0, 5], [0, 5], dtype=7) == _lib.ZL_EUNSUPPORTED
+    assert _fwd(lib, [0, 5], [0, 5], scale=-1.0) == _lib.ZL_EINVAL
+    assert _fwd(lib, [0, 5], [0, 5], scale=float("nan")) == _lib.ZL_EINVAL
+    assert _fwd(lib, [0, 5], [0, 5], ptr=8) == _lib.ZL_EALIGN
+    assert _fwd(lib, [0, 5], [0, 5], ptr=0) == _lib.ZL_EINVAL
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert _fwd(lib, [0], [0], ptr=0) == _lib.ZL_OK
+    assert _fwd(lib, [0, 0, 0], [0, 0, 0], ptr=0) == _lib.ZL_OK
+
+
+def test_tile_table_validation(lib):
+    L = 300
+    good = synth.grid_tiles(0, L, L, 2, 3)
+    cu = [0, L, L + 10]
+
+    def ws_size(tiles):
+        cq, nq = _lib.int32_array(cu)
+        ta, nt = _lib.tile_array(tiles)
+        out = ctypes.c_size_t(0)
+        st = lib.zl_varlen_attn_fwd_workspace_size(cq, cq, nq - 1, 2, 64, ta, nt, ctypes.byref(out))
+        return st, out.value
+
+    st, nbytes = ws_size(good)
+    assert st == _lib.ZL_OK
+    assert nbytes >= 3 * L * 2 * 64 * 4 + 3 * 2 * L * 4
+    assert ws_size(list(reversed(good)))[0] == _lib.ZL_OK            # any order
+    assert ws_size(good[:-1])[0] == _lib.ZL_EINVAL                   # missing tile
+    assert ws_size(good + [good[0]])[0] == _lib.ZL_EINVAL            # duplicate
+    bad = list(good)
+    t = list(bad[1]); t[4] -= 1; bad[1] = tuple(t)                   # gap in key range
+    assert ws_size(bad)[0] == _lib.ZL_EINVAL
+    bad = list(good)
+    t = list(bad[0]); t[7] = 4; bad[0] = tuple(t)                    # n_kv mismatch
+    assert ws_size(bad)[0] == _lib.ZL_EINVAL
+    bad = list(good)
+    t = list(bad[0]); t[0] = 5; bad[0] = tuple(t)                    # seq out of range
+    assert ws_size(bad)[0] == _lib.ZL_EINVAL
+    # a full grid whose query chunks do not cover the sequence
+    assert ws_size(synth.grid_tiles(0, L - 1, L, 2, 3))[0] == _lib.ZL_EINVAL
+    # a sequence with an empty chunk (4 chunks of 1 token over 3 tokens) is rejected
+    assert ws_size([(1, 0, 10, 0, 10, 0, 0, 1)])[0] == _lib.ZL_OK
+    assert _fwd(lib, cu, cu, tiles=good, ws=0) == _lib.ZL_EWORKSPACE
+    assert _fwd(lib, cu, cu, tiles=good, ws=256, ws_bytes=16) == _lib.ZL_EWORKSPACE
+
+
+def test_workspace_size_matches_layout(lib):
+    wl = synth.config(4)
+    cq, nq = _lib.int32_array(wl.cu_seqlens())
+    ta, nt = _lib.tile_array(wl.tiles())
+    out = ctypes.c_size_t(0)
+    assert lib.zl_varlen_attn_fwd_workspace_size(cq, cq, nq - 1, 40, 128, ta, nt, ctypes.byref(out)) == 0
+    R, P = 131072, 4
+    assert out.value == P * R * 40 * 128 * 4 + P * 40 * R * 4
+    out2 = ctypes.c_size_t(0)
+    assert lib.zl_varlen_attn_bwd_workspace_size(cq, cq, nq - 1, 40, 128, ctypes.byref(out2)) == 0
+    T = wl.total_tokens
+    assert out2.value >= T * 40 * 128 * 4 + 40 * T * 4
+
+
+def test_merge_argument_checks(lib):
+    p = ctypes.c_void_p(64)
+    assert lib.zl_lse_merge(p, p, 0, 10, 2, 64, 10, p, 0, p, 10, None) == _lib.ZL_EINVAL
+    assert lib.zl_lse_merge(p, p, 65, 10, 2, 64, 10, p, 0, p, 10, None) == _lib.ZL_EINVAL
+    assert lib.zl_lse_merge(p, p, 2, 10, 2, 64, 5, p, 0, p, 10, None) == _lib.ZL_EINVAL
+    assert lib.zl_lse_merge(p, p, 2, 10, 2, 32, 10, p, 0, p, 10, None) == _lib.ZL_EUNSUPPORTED
+    assert lib.zl_lse_merge(p, p, 2, 0, 2, 64, 0, p, 0, p, 0, None) == _lib.ZL_OK
+
+
+def test_bwd_argument_checks(lib):
+    cq, nq = _lib.int32_array([0, 5])
+    p = ctypes.c_void_p(64)
+    args = [p] * 6 + [cq, cq, nq - 1, 2, 64]
+    tail = [None, 0, p, p, p, p, 1 << 20, None]
+    assert lib.zl_varlen_attn_bwd(*args, _lib.ZL_FP32, 0.125, *tail) == _lib.ZL_EUNSUPPORTED
+    assert lib.zl_varlen_attn_bwd(*args, _lib.ZL_BF16, 0.0, *tail) == _lib.ZL_EINVAL
+
+
+def test_no_device_is_reported_not_crashed(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _fwd(lib, [0, 5], [0, 5]) == _lib.ZL_ENODEVICE

@@ -1,0 +1,210 @@
+"""Forward parity on the GPU: the CUDA path through the C ABI against the
+float64 oracle on the same seeded inputs.
+
+The operation is the coalesced block-diagonal attention of Zellige
+(arXiv 2608.01150v1) §IV-D, with shards of split sequences computed as
+(query-chunk x KV-chunk) tiles and merged exactly (§II-B, Table II).
+Tolerances: bf16 O max-abs 2e-2 and LSE 1e-3 against float64; float32 mode
+1e-4.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import mixed_length_dit_gb300 as zl
+from _helpers import TOL_FP32, TOL_LSE, TOL_O_BF16, f64, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(inp, wl, tiles=None, cu_q=None, cu_k=None):
+    cu = wl.cu_seqlens()
+    o, lse = zl.varlen_attn_fwd(inp["q"], inp["k"], inp["v"], cu_q or cu, cu_k or cu, tiles=tiles)
+    zl.sync_check()
+    return o, lse
+
+
+def _full_check(q, k, v, cu_q, cu_k, o, lse, tol_o, tol_lse):
+    o_ref, lse_ref = oracle.varlen_attn_fwd(f64(q), f64(k), f64(v), cu_q, cu_k)
+    err_o = np.abs(f64(o) - o_ref).max()
+    mask = np.isfinite(lse_ref)
+    err_l = np.abs(f64(lse)[mask] - lse_ref[mask]).max() if mask.any() else 0.0
+    assert err_o <= tol_o, f"O max-abs {err_o}"
+    assert err_l <= tol_lse, f"LSE max-abs {err_l}"
+    return err_o, err_l
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_tiny_bf16(split):
+    wl = synth.config(1)
+    inp = synth.make_inputs(wl, seed=0, device="cuda", with_grad_out=False)
+    tiles = None
+    if split:
+        tiles = synth.grid_tiles(3, 256, 256, 2, 2) + synth.grid_tiles(2, 100, 100, 3, 2)
+    o, lse = _run(inp, wl, tiles)
+    cu = wl.cu_seqlens()
+    _full_check(inp["q"], inp["k"], inp["v"], cu, cu, o, lse, TOL_O_BF16, TOL_LSE)
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_tiny_fp32(split):
+    wl = synth.config(1)
+    inp = synth.make_inputs(wl, seed=0, device="cuda", dtype=torch.float32, with_grad_out=False)
+    tiles = synth.grid_tiles(3, 256, 256, 2, 2) if split else None
+    o, lse = _run(inp, wl, tiles)
+    assert o.dtype == torch.float32
+    cu = wl.cu_seqlens()
+    _full_check(inp["q"], inp["k"], inp["v"], cu, cu, o, lse, TOL_FP32, TOL_FP32)
+
+
+@pytest.mark.parametrize("hd", [64, 128])
+def test_ragged_edges(hd):
+    """Lengths around the 128-row block: 1, 2, 127, 128, 129, 255, 257, an
+    empty sequence, and a short tail."""
+    lens = [1, 2, 127, 128, 129, 0, 255, 257, 3]
+    wl = synth.Workload("edges", lens, 3, hd)
+    inp = synth.make_inputs(wl, seed=5, device="cuda", with_grad_out=False)
+    o, lse = _run(inp, wl)
+    cu = wl.cu_seqlens()
+    _full_check(inp["q"], inp["k"], inp["v"], cu, cu, o, lse, TOL_O_BF16, TOL_LSE)
+
+
+def test_different_query_and_key_lengths():
+    cu_q = [0, 5, 200, 330]
+    cu_k = [0, 130, 140, 600]
+    g = torch.Generator(device="cuda").manual_seed(9)
+    q = torch.randn((330, 2, 128), generator=g, device="cuda").to(torch.bfloat16)
+    k = torch.randn((600, 2, 128), generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn((600, 2, 128), generator=g, device="cuda").to(torch.bfloat16)
+    o, lse = zl.varlen_attn_fwd(q, k, v, cu_q, cu_k)
+    zl.sync_check()
+    _full_check(q, k, v, cu_q, cu_k, o, lse, TOL_O_BF16, TOL_LSE)
+    # the same batch with sequence 2 split into a 2 x 3 grid of tiles
+    tiles = synth.grid_tiles(2, 130, 460, 2, 3)
+    o2, lse2 = zl.varlen_attn_fwd(q, k, v, cu_q, cu_k, tiles=tiles)
+    zl.sync_check()
+    _full_check(q, k, v, cu_q, cu_k, o2, lse2, TOL_O_BF16, TOL_LSE)
+
+
+def test_image_mix_full():
+    """Image-only mix: 16 x 256 + 8 x 1024 + 4 x 4096 tokens, 24 heads, d = 128,
+    every row and head against the oracle."""
+    wl = synth.config(2)
+    inp = synth.make_inputs(wl, seed=0, device="cuda", with_grad_out=False)
+    o, lse = _run(inp, wl)
+    cu = wl.cu_seqlens()
+    _full_check(inp["q"], inp["k"], inp["v"], cu, cu, o, lse, TOL_O_BF16, TOL_LSE)
+
+
+def _sampled_check(wl, inp, o, lse, seed=0, n_random=2048, max_heads_long=4):
+    """Row-sampled parity: rows are independent, so the oracle's value for a
+    sampled row is exactly the full call's value for it."""
+    rng = np.random.default_rng(seed)
+    cu = wl.cu_seqlens()
+    splits = wl.splits
+    worst_o = worst_l = 0.0
+    cache = {}
+    for s, L in enumerate(wl.seqlens):
+        if L == 0:
+            continue
+        nq = splits.get(s, (1, 1))[0]
+        rows = sample_rows(L, synth.chunk_bounds(L, nq), n_random, rng)
+        heads = list(range(wl.num_heads))
+        if L > 32768:
+            heads = sorted(set([0, wl.num_heads - 1] + list(rng.choice(wl.num_heads, max_heads_long - 2,
+                                                                        replace=False))))
+        a, b = cu[s], cu[s + 1]
+        key = (L, tuple(rows.tolist()))
+        qs = f64(inp["q"][a:b])
+        ks = f64(inp["k"][a:b])
+        vs = f64(inp["v"][a:b])
+        cu1 = [0, L]
+        og = f64(o[a:b])
+        lg = f64(lse[:, a:b])
+        for h in heads:
+            o_ref, l_ref = oracle.attention_rows(qs, ks, vs, cu1, cu1, 0, h, rows)
+            worst_o = max(worst_o, float(np.abs(og[rows, h] - o_ref).max()))
+            worst_l = max(worst_l, float(np.abs(lg[h, rows] - l_ref).max()))
+        cache[key] = True
+    assert worst_o <= TOL_O_BF16, worst_o
+    assert worst_l <= TOL_LSE, worst_l
+    return worst_o, worst_l
+
+
+def test_wan_mix_sampled():
+    wl = synth.config(3)
+    inp = synth.make_inputs(wl, seed=0, device="cuda", with_grad_out=False)
+    o, lse = _run(inp, wl)
+    _sampled_check(wl, inp, o, lse, n_random=1024)
+
+
+def test_shard_mode_131k():
+    """One 131,072-token sequence as 4 x 4 tiles beside 64 images of 1024
+    tokens in one launch, then the merge: equals the same batch run whole, and
+    the oracle on sampled rows."""
+    wl = synth.config(4)
+    inp = synth.make_inputs(wl, seed=0, device="cuda", with_grad_out=False)
+    o, lse = _run(inp, wl, wl.tiles())
+    _sampled_check(wl, inp, o, lse, n_random=512, max_heads_long=3)
+    o_whole, lse_whole = _run(inp, wl, None)
+    assert (o - o_whole).abs().max().item() <= TOL_O_BF16
+    assert (lse - lse_whole).abs().max().item() <= TOL_LSE
+    # images are not split: identical work items, identical bits
+    a = wl.seqlens[0]
+    assert torch.equal(o[a:], o_whole[a:])
+
+
+def test_train_step_mix_sampled():
+    wl = synth.config(5)
+    inp = synth.make_inputs(wl, seed=0, device="cuda", with_grad_out=False)
+    o, lse = _run(inp, wl, wl.tiles())
+    _sampled_check(wl, inp, o, lse, n_random=512, max_heads_long=3)
+
+
+def test_sequence_isolation_bitwise():
+    """§IV-D keeps sequences separate: changing one sequence's q/k/v leaves
+    every other sequence's output bit-identical; outputs stay in input order."""
+    wl = synth.Workload("iso", [300, 64, 1000, 129], 4, 128)
+    inp = synth.make_inputs(wl, seed=2, device="cuda", with_grad_out=False)
+    o1, l1 = _run(inp, wl)
+    cu = wl.cu_seqlens()
+    inp2 = {k2: t.clone() for k2, t in inp.items()}
+    a, b = cu[2], cu[3]
+    inp2["k"][a:b] += 1.0
+    inp2["v"][a:b] *= -1
+    o2, l2 = _run(inp2, wl)
+    for s in (0, 1, 3):
+        x, y = cu[s], cu[s + 1]
+        assert torch.equal(o1[x:y], o2[x:y])
+        assert torch.equal(l1[:, x:y], l2[:, x:y])
+    assert not torch.equal(o1[a:b], o2[a:b])
+
+
+@pytest.mark.parametrize("hd,out_dtype", [(64, torch.float32), (128, torch.bfloat16),
+                                          (128, torch.float32)])
+def test_lse_merge_standalone(hd, out_dtype):
+    g = torch.Generator(device="cuda").manual_seed(11)
+    P, R, H = 3, 777, 5
+    o_part = torch.randn((P, R, H, hd), generator=g, device="cuda")
+    lse_part = 4 * torch.randn((P, H, R), generator=g, device="cuda")
+    lse_part[1, :, 10:20] = float("-inf")        # an empty partial
+    lse_part[:, 2, 30:33] = float("-inf")        # rows with nothing at all
+    o, lse = zl.lse_merge(o_part, lse_part, out_dtype=out_dtype)
+    zl.sync_check()
+    o_ref, l_ref = oracle.lse_merge(f64(o_part), f64(lse_part))
+    tol = TOL_O_BF16 if out_dtype == torch.bfloat16 else 1e-5
+    assert np.abs(f64(o) - o_ref).max() <= tol
+    fin = np.isfinite(l_ref)
+    assert np.abs(f64(lse)[fin] - l_ref[fin]).max() <= 1e-5
+    assert np.all(np.isneginf(f64(lse)[~fin]))
+    assert np.all(f64(o)[30:33, 2] == 0)
+
+
+def test_launch_counter_and_no_errors():
+    wl = synth.config(1)
+    inp = synth.make_inputs(wl, seed=0, device="cuda", with_grad_out=False)
+    n0 = zl.launch_count()
+    _run(inp, wl, synth.grid_tiles(3, 256, 256, 2, 2))
+    assert zl.launch_count() - n0 == 2     # one attention launch + one merge

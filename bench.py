@@ -1,0 +1,442 @@
+"""Benchmark of the coalesced varlen attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 1..5] [--mode step|fwd]
+
+One step = one pass of the whole path over one batch: the forward over whole
+sequences and shard tiles in one launch, the exact LSE merge of the tiles, the
+backward preprocess, the backward, and the dQ conversion.  The default
+workload is the training-step batch (a 720p 81-frame video of 75,600 tokens
+split into a 2 x 2 tile grid, two 480p 81-frame videos of 32,760 tokens, four
+4,096-token and 32 1,024-token images; 40 heads, head dim 128, bf16).
+
+The metric is attention TFLOP/s: algorithmic FLOPs (forward 4 * sum(Lq * Lk)
+* d * H; forward + backward 3.5x that) over device time, timed with CUDA
+events over exactly K steps after W warm-up steps.  Every input tensor is
+larger than L2 (129 MB), so no L2 flush is needed between steps.
+
+With torchrun (N > 1) every rank runs an independent replica of the same
+workload on its own GPU (the path has no cross-GPU exchange); the time is the
+maximum over ranks and the value is the work of all ranks over that time.
+
+--impl reference times the float64 CPU oracle (the correctness reference) on a
+bounded sample of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "varlen attn TFLOP/s (fwd; fwd+bwd) on mixed image-video batch, % of BF16 peak"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
+CSRC = os.path.join(ROOT, "mixed_length_dit_gb300", "csrc")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- helpers
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(name: str) -> str:
+    with open(os.path.join(CSRC, name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from an ncu capture (profiles/traffic.txt), or
+    None when missing or taken on a different version of the kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return None
+    src = {"fwd_tc": "fwd_tc.cu", "bwd_tc": "bwd_tc.cu", "lse_merge": "merge.cu"}.get(kernel)
+    if src is None:
+        return None
+    h = source_hash(src)
+    for line in lines:
+        if line.startswith("#") or not line.strip():
+            continue
+        f = dict(x.split("=", 1) for x in line.split())
+        if f.get("kernel") == kernel and f.get("workload") == workload and f.get("src") == h:
+            return float(f["bytes_per_launch"])
+    return None
+
+
+def workload_desc(wl) -> str:
+    counts = {}
+    for n in wl.seqlens:
+        counts[n] = counts.get(n, 0) + 1
+    parts = []
+    for n, c in sorted(counts.items(), key=lambda x: -x[0]):
+        parts.append(f"{c}x{n}")
+    split = ", ".join(f"seq {s} ({wl.seqlens[s]} tokens) as {a}x{b} tiles" for s, (a, b) in wl.splits.items())
+    return (f"{wl.name}: " + " + ".join(parts) + f" tokens; H={wl.num_heads}, d={wl.head_dim}"
+            + (f"; {split}" if split else ""))
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.path = tempfile.mktemp(prefix="zl_clocks_", suffix=".csv")
+        self.proc = None
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", gpu_index], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def gpu_index_for_smi(local_rank: int) -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(ids) and ids[local_rank].isdigit():
+            return ids[local_rank]
+    return str(local_rank)
+
+
+def fwd_flops(wl) -> float:
+    return 4.0 * wl.head_dim * wl.num_heads * wl.pair_count()
+
+
+def merge_bytes(wl, launch_rows) -> float:
+    """Algorithmic bytes of one merge launch over `launch_rows` query rows."""
+    nparts = max(b for _, b in wl.splits.values())
+    h, d = wl.num_heads, wl.head_dim
+    return launch_rows * h * (nparts * (4 * d + 4) + (2 * d + 4))
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_sample(wl, inp, target_tokens: int, n_heads: int):
+    """The first `n_heads` heads of the sequence of the workload nearest
+    `target_tokens` long, copied to float64 host arrays, and their algorithmic
+    fwd+bwd FLOPs."""
+    lens = wl.seqlens
+    s = min(range(len(lens)), key=lambda i: (abs(lens[i] - target_tokens), i))
+    cu = wl.cu_seqlens()
+    a, b = cu[s], cu[s + 1]
+    n_heads = min(n_heads, wl.num_heads)
+    arrs = [inp[n][a:b, :n_heads].to("cpu", torch.float64).numpy() for n in ("q", "k", "v", "do")]
+    L = b - a
+    return arrs, L, n_heads, n_heads * 3.5 * 4.0 * L * L * wl.head_dim
+
+
+def time_oracle(arrs, L):
+    import oracle
+    q, k, v, do = arrs
+    cu = [0, L]
+    t0 = time.perf_counter()
+    oracle.varlen_attn_fwd(q, k, v, cu, cu)
+    oracle.varlen_attn_bwd(q, k, v, do, cu, cu)
+    return time.perf_counter() - t0
+
+
+def cpu_threads() -> int:
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=5)
+    ap.add_argument("--mode", choices=["step", "fwd"], default="step")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-tokens", type=int, default=4096,
+                    help="length of the sequence whose heads the CPU oracle times")
+    ap.add_argument("--oracle-heads", type=int, default=16,
+                    help="number of heads of that sequence the CPU oracle times")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = synth.config(args.workload)
+    peaks, peak_kind = load_peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args, wl, world)
+
+    import torch.distributed as dist
+    import mixed_length_dit_gb300 as zl
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank)
+    inp = synth.make_inputs(wl, seed=rank, device=dev)
+    cu = wl.cu_seqlens()
+    tiles = wl.tiles() or None
+    H, D, T = wl.num_heads, wl.head_dim, wl.total_tokens
+    o = torch.empty_like(inp["q"])
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    fws = zl.alloc_workspace(zl.fwd_workspace_bytes(cu, cu, H, D, tiles), dev)
+    dq, dk, dv = (torch.empty_like(inp["q"]) for _ in range(3))
+    bws = zl.alloc_workspace(zl.bwd_workspace_bytes(cu, cu, H, D), dev)
+    step_bwd = args.mode == "step"
+
+    def step(q, k, v, do):
+        zl.varlen_attn_fwd(q, k, v, cu, cu, tiles=tiles, out=o, lse=lse, workspace=fws)
+        if step_bwd:
+            zl.varlen_attn_bwd(q, k, v, o, lse, do, cu, cu, tiles=tiles, dq=dq, dk=dk, dv=dv, workspace=bws)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step(inp["q"], inp["k"], inp["v"], inp["do"])
+    zl.sync_check()
+
+    sampler = ClockSampler(gpu_index_for_smi(local_rank))
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    n_launch0 = zl.launch_count()
+    zl.profile_begin()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step(inp["q"], inp["k"], inp["v"], inp["do"])
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    prof = zl.profile_end()
+    clocks = sampler.stop()
+    launches = zl.launch_count() - n_launch0
+    zl.sync_check()
+    ms_local = e0.elapsed_time(e1)
+    ms = torch.tensor([ms_local], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
+    ms_total = float(ms.item())
+    flops_fwd = fwd_flops(wl)
+    flops_step = flops_fwd * (3.5 if step_bwd else 1.0)
+    value = world * args.steps * flops_step / (ms_total * 1e-3) / 1e12
+
+    # ---------------- per-kernel roofline of the dominant kernel
+    dom = max(prof.items(), key=lambda kv: kv[1][1])[0] if prof else None
+    roof = None
+    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    if dom is not None:
+        n_l, tot = prof[dom]
+        avg_ms = tot / n_l
+        traffic = recorded_traffic(dom, wl.name)
+        if dom in ("fwd_tc", "bwd_tc"):
+            per_launch = (flops_fwd if dom == "fwd_tc" else 2.5 * flops_fwd) * args.steps / n_l
+            ach = per_launch / (avg_ms * 1e-3) / 1e12
+            roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": sustained, "unit": "TFLOP/s",
+                    "frac": round(ach / sustained, 4), "traffic": traffic,
+                    "kernel": dom, "peak_kind": f"bf16 sustained ({peak_kind})",
+                    "flops_per_launch": per_launch, "avg_launch_ms": round(avg_ms, 4)}
+        else:
+            hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+            rows = sum(wl.seqlens[s] for s in wl.splits)
+            per_launch = merge_bytes(wl, rows) * args.steps / max(1, n_l)
+            ach = per_launch / (avg_ms * 1e-3) / 1e9
+            roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(ach / hbm, 4), "traffic": traffic, "kernel": dom}
+    kernels = {k: {"launches": v[0], "avg_ms": round(v[1] / v[0], 4),
+                   "share": round(v[1] / sum(x[1] for x in prof.values()), 4)} for k, v in prof.items()}
+    fwd_ms = sum(prof[k][1] for k in ("fwd_tc", "lse_merge") if k in prof) / args.steps
+    bwd_ms = sum(prof[k][1] for k in ("bwd_preprocess", "bwd_tc", "dq_convert") if k in prof) / args.steps
+    phases = {"fwd_tflops": round(flops_fwd / (fwd_ms * 1e-3) / 1e12, 1) if fwd_ms else None}
+    if step_bwd and bwd_ms:
+        phases["bwd_tflops"] = round(2.5 * flops_fwd / (bwd_ms * 1e-3) / 1e12, 1)
+
+    # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = {n: inp[n].to("cpu").pin_memory() for n in ("q", "k", "v", "do")}
+        host_out = {n: torch.empty(inp["q"].shape, dtype=inp["q"].dtype).pin_memory()
+                    for n in (("o", "dq", "dk", "dv") if step_bwd else ("o",))}
+        dev_in = {n: torch.empty_like(inp[n]) for n in host_in}
+        srcs = {"o": o, "dq": dq, "dk": dk, "dv": dv}
+        k_e2e = max(1, min(args.steps, 5))
+
+        def e2e_step():
+            for n in host_in:
+                dev_in[n].copy_(host_in[n], non_blocking=True)
+            step(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["do"])
+            for n in host_out:
+                host_out[n].copy_(srcs[n], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record()
+        for _ in range(k_e2e):
+            e2e_step()
+        f1.record()
+        torch.cuda.synchronize()
+        barrier()
+        ems = torch.tensor([f0.elapsed_time(f1)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(ems, op=dist.ReduceOp.MAX)
+        bi = sum(t.numel() * t.element_size() for t in host_in.values())
+        bo = sum(t.numel() * t.element_size() for t in host_out.values())
+        e2e = {"value": round(world * k_e2e * flops_step / (float(ems.item()) * 1e-3) / 1e12, 1),
+               "unit": "TFLOP/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": k_e2e}
+        del dev_in, host_in, host_out
+
+    # ---------------- CPU oracle baseline (rank 0, single GPU)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        arrs, L, nh_s, fl = oracle_sample(wl, inp, args.oracle_tokens, args.oracle_heads)
+        secs = time_oracle(arrs, L)
+        cpu = {"value": round(fl / secs / 1e12, 5), "unit": "TFLOP/s", "cores": cpu_threads(),
+               "kind": "oracle",
+               "sample": f"float64 numpy oracle, fwd+bwd of {nh_s} heads of one {L}-token sequence of the "
+                         f"workload ({fl / 1e12:.3f} TFLOP algorithmic) in {secs:.1f} s"}
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    bf16_peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_total / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: q, k, v, dO ~ N(0,1) drawn in float32 from a seeded generator, rounded to bf16",
+        "config": {"workload": workload_desc(wl), "mode": "fwd+bwd step" if step_bwd else "fwd only",
+                   "total_tokens": wl.total_tokens, "sequences": len(wl.seqlens),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "no flush: every input tensor (>= %.2f GB) is larger than the 129 MB L2"
+                         % (wl.total_tokens * H * D * 2 / 1e9),
+                   "flops_per_step": flops_step},
+        "pct_of_peak": round(100 * value / world / bf16_peak, 2),
+        "peak_tflops": bf16_peak,
+        "phases": phases,
+        "kernels": kernels,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reference(args, wl, world):
+    """The float64 CPU oracle, as it stands, on a bounded sample of the same
+    workload: each step is the fwd+bwd of one head of one sequence."""
+    g = torch.Generator().manual_seed(0)
+    target = 4096
+    lens = wl.seqlens
+    s = min(range(len(lens)), key=lambda i: (abs(lens[i] - target), i))
+    L = lens[s]
+    arrs = [torch.randn((L, 1, wl.head_dim), generator=g).to(torch.bfloat16).double().numpy() for _ in range(4)]
+    fl = 3.5 * 4.0 * L * L * wl.head_dim
+    for _ in range(args.warmup):
+        time_oracle(arrs, L)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time_oracle(arrs, L)
+    secs = time.perf_counter() - t0
+    value = args.steps * fl / secs / 1e12
+    sample = (f"float64 numpy oracle, fwd+bwd of one head of one {L}-token sequence of the workload "
+              f"({fl / 1e9:.1f} GFLOP algorithmic) per step")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 5),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic: N(0,1) rounded to bf16, upcast to float64",
+        "config": {"workload": workload_desc(wl), "mode": "fwd+bwd step (sampled)"},
+        "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -203,6 +203,25 @@ zl_status zl_sync_check(void* stream);
 /* Number of kernel launches this library has enqueued in this process. */
 int64_t zl_launch_count(void);
 
+/*
+ * Per-kernel timing, the single-GPU counterpart of the paper's Hardware
+ * Profiler, which measures execution time per configuration (Zellige §IV-B).
+ * Between zl_profile_begin() and zl_profile_end() every kernel this library
+ * launches is bracketed by two CUDA events on its stream.  zl_profile_end()
+ * waits for those events, writes one entry per kernel name (launch count and
+ * summed device time) into `entries` (up to max_entries; *n_entries gets the
+ * number written), releases the events and stops recording.  Recording is
+ * process-wide; begin while already recording returns ZL_EINVAL.
+ */
+typedef struct {
+  char name[32];
+  int64_t launches;
+  double total_ms;
+} zl_profile_entry_t;
+
+zl_status zl_profile_begin(void);
+zl_status zl_profile_end(zl_profile_entry_t* entries, int32_t max_entries, int32_t* n_entries);
+
 #ifdef __cplusplus
 }
 #endif

@@ -6,6 +6,6 @@ binding (attention.py).
 """
 from .attention import (  # noqa: F401
     alloc_workspace, bwd_workspace_bytes, fwd_workspace_bytes, launch_count, lse_merge,
-    sync_check, varlen_attn_bwd, varlen_attn_fwd,
+    profile_begin, profile_end, sync_check, varlen_attn_bwd, varlen_attn_fwd,
 )
 from ._lib import ZlError, load  # noqa: F401

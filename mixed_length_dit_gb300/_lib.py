@@ -28,7 +28,7 @@ ZL_FP32 = 1
 EXPORTS = (
     "zl_status_string", "zl_version", "zl_varlen_attn_fwd_workspace_size", "zl_varlen_attn_fwd",
     "zl_lse_merge", "zl_varlen_attn_bwd_workspace_size", "zl_varlen_attn_bwd", "zl_sync_check",
-    "zl_launch_count",
+    "zl_launch_count", "zl_profile_begin", "zl_profile_end",
 )
 
 
@@ -36,6 +36,11 @@ class Tile(ctypes.Structure):
     """zl_tile_t"""
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("seq", "q_start", "q_len", "k_start", "k_len", "q_chunk", "kv_chunk", "n_kv_chunks")]
+
+
+class ProfileEntry(ctypes.Structure):
+    """zl_profile_entry_t"""
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
 
 
 class ZlError(RuntimeError):
@@ -80,6 +85,10 @@ def load() -> ctypes.CDLL:
     lib.zl_varlen_attn_bwd.restype = c_i32
     lib.zl_varlen_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i32p, i32p, c_i32, c_i32, c_i32, c_i32,
                                        c_f32, tilep, c_i32, vp, vp, vp, vp, c_sz, vp]
+    lib.zl_profile_begin.restype = c_i32
+    lib.zl_profile_begin.argtypes = []
+    lib.zl_profile_end.restype = c_i32
+    lib.zl_profile_end.argtypes = [ctypes.POINTER(ProfileEntry), c_i32, ctypes.POINTER(c_i32)]
     _lib = lib
     return lib
 

@@ -151,3 +151,17 @@ def sync_check(stream=None) -> None:
 
 def launch_count() -> int:
     return int(_lib.load().zl_launch_count())
+
+
+def profile_begin() -> None:
+    """Starts per-kernel event timing of this library's launches."""
+    _lib.check(_lib.load().zl_profile_begin(), "zl_profile_begin")
+
+
+def profile_end() -> dict:
+    """Stops timing; returns {kernel name: (launches, total device ms)}."""
+    lib = _lib.load()
+    arr = (_lib.ProfileEntry * 32)()
+    n = ctypes.c_int32(0)
+    _lib.check(lib.zl_profile_end(arr, 32, ctypes.byref(n)), "zl_profile_end")
+    return {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms)) for i in range(n.value)}

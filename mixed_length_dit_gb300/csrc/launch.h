@@ -90,7 +90,7 @@ cudaError_t launch_fwd_f32(int head_dim, const float* q, const float* k, const f
                            const FwdArgs& args, cudaStream_t stream);
 cudaError_t launch_merge(int head_dim, const MergeArgs& args, int num_sms, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(int head_dim, const void* o, const void* dout, float* dsum,
-                                  int64_t tq, int32_t num_heads, int num_sms,
+                                  float* dq_acc, int64_t tq, int32_t num_heads, int num_sms,
                                   cudaStream_t stream);
 cudaError_t launch_bwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,

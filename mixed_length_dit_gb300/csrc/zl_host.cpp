@@ -34,6 +34,58 @@ using zl::kMaxSegs;
 
 std::atomic<int64_t> g_launches{0};
 
+// ------------------------------------------------------------------ profiling
+struct ProfRecord {
+  const char* name;
+  cudaEvent_t start;
+  cudaEvent_t stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRecord> g_prof;
+
+// Launches through `fn`, counting it and, while profiling, bracketing it with
+// events on `stream`.
+template <typename F>
+zl_status launch_counted(const char* name, cudaStream_t stream, F fn) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  bool prof = false;
+  {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    prof = g_prof_on;
+  }
+  if (prof) {
+    if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess ||
+        cudaEventRecord(a, stream) != cudaSuccess) {
+      cudaGetLastError();
+      if (a) cudaEventDestroy(a);
+      if (b) cudaEventDestroy(b);
+      return ZL_ECUDA;
+    }
+  }
+  const cudaError_t e = fn();
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    if (prof) {
+      cudaEventDestroy(a);
+      cudaEventDestroy(b);
+    }
+    return ZL_ECUDA;
+  }
+  g_launches.fetch_add(1);
+  if (prof) {
+    if (cudaEventRecord(b, stream) != cudaSuccess) {
+      cudaGetLastError();
+      cudaEventDestroy(a);
+      cudaEventDestroy(b);
+      return ZL_ECUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof.push_back(ProfRecord{name, a, b});
+  }
+  return ZL_OK;
+}
+
 // ------------------------------------------------------------------ device
 struct DevInfo {
   int sms = 0;
@@ -347,9 +399,8 @@ zl_status zl_lse_merge(const float* o_partial, const float* lse_partial, int32_t
   a.n_parts = n_parts;
   a.num_heads = num_heads;
   a.out_bf16 = out_dtype == ZL_BF16 ? 1 : 0;
-  st = cuda_status(zl::launch_merge(head_dim, a, sms, static_cast<cudaStream_t>(stream)));
-  if (st == ZL_OK) g_launches.fetch_add(1);
-  return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return launch_counted("lse_merge", s, [&] { return zl::launch_merge(head_dim, a, sms, s); });
 }
 
 zl_status zl_varlen_attn_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
@@ -399,17 +450,16 @@ zl_status zl_varlen_attn_fwd(const void* q, const void* k, const void* v, const 
     const size_t last = std::min(segs.size(), first + kMaxSegs);
     fill_args(&args, segs, first, last, num_heads);
     if (args.n_items == 0) continue;
-    cudaError_t e;
     if (dtype == ZL_BF16) {
       const int grid = std::min(args.n_items, 2 * sms);
-      e = zl::launch_fwd_tc(head_dim, mq, mk, mv, args, grid, s);
+      st = launch_counted("fwd_tc", s, [&] { return zl::launch_fwd_tc(head_dim, mq, mk, mv, args, grid, s); });
     } else {
-      e = zl::launch_fwd_f32(head_dim, static_cast<const float*>(q), static_cast<const float*>(k),
-                             static_cast<const float*>(v), args, s);
+      st = launch_counted("fwd_f32", s, [&] {
+        return zl::launch_fwd_f32(head_dim, static_cast<const float*>(q), static_cast<const float*>(k),
+                                  static_cast<const float*>(v), args, s);
+      });
     }
-    st = cuda_status(e);
     if (st != ZL_OK) return st;
-    g_launches.fetch_add(1);
   }
   // Combine each split sequence's partial slots into its rows of o and lse.
   const size_t esz = dtype == ZL_BF16 ? 2 : 4;
@@ -425,9 +475,8 @@ zl_status zl_varlen_attn_fwd(const void* q, const void* k, const void* v, const 
     m.n_parts = sp.n_kv;
     m.num_heads = num_heads;
     m.out_bf16 = dtype == ZL_BF16 ? 1 : 0;
-    st = cuda_status(zl::launch_merge(head_dim, m, sms, s));
+    st = launch_counted("lse_merge", s, [&] { return zl::launch_merge(head_dim, m, sms, s); });
     if (st != ZL_OK) return st;
-    g_launches.fetch_add(1);
   }
   return ZL_OK;
 }
@@ -449,14 +498,140 @@ zl_status zl_varlen_attn_bwd(const void* q, const void* k, const void* v, const 
                              int32_t num_seqs, int32_t num_heads, int32_t head_dim, int32_t dtype,
                              float softmax_scale, const zl_tile_t* tiles, int32_t num_tiles, void* dq,
                              void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
-  (void)q; (void)k; (void)v; (void)o; (void)lse; (void)dout; (void)dq; (void)dk; (void)dv;
-  (void)workspace; (void)workspace_bytes; (void)stream;
   if (dtype != ZL_BF16) return ZL_EUNSUPPORTED;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return ZL_EINVAL;
   Plan plan;
-  const zl_status st = make_plan(cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, tiles, num_tiles, &plan);
+  zl_status st = make_plan(cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, tiles, num_tiles, &plan);
   if (st != ZL_OK) return st;
-  return ZL_EUNSUPPORTED;
+  if (plan.tq == 0 && plan.tk == 0) return ZL_OK;
+  if ((plan.tq > 0 && (!q || !o || !lse || !dout || !dq)) || (plan.tk > 0 && (!k || !v || !dk || !dv)))
+    return ZL_EINVAL;
+  const void* ptrs[] = {q, k, v, o, dout, dq, dk, dv, lse};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return ZL_EALIGN;
+  const size_t dq_bytes = align256(static_cast<size_t>(plan.tq) * num_heads * head_dim * sizeof(float));
+  const size_t need = dq_bytes + align256(static_cast<size_t>(plan.tq) * num_heads * sizeof(float));
+  if (plan.tq > 0 && (!workspace || workspace_bytes < need)) return ZL_EWORKSPACE;
+  if (plan.tq > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ZL_EALIGN;
+  int sms = 0;
+  st = device_sms(&sms);
+  if (st != ZL_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t row_bytes = static_cast<size_t>(num_heads) * head_dim * 2;
+
+  // Keys of sequences without queries get zero gradients.
+  for (int32_t i = 0; i < num_seqs; ++i) {
+    const int32_t lq = cu_seqlens_q[i + 1] - cu_seqlens_q[i];
+    const int32_t lk = cu_seqlens_k[i + 1] - cu_seqlens_k[i];
+    if (lq == 0 && lk > 0) {
+      st = cuda_status(cudaMemsetAsync(static_cast<char*>(dk) + cu_seqlens_k[i] * row_bytes, 0, lk * row_bytes, s));
+      if (st == ZL_OK)
+        st = cuda_status(cudaMemsetAsync(static_cast<char*>(dv) + cu_seqlens_k[i] * row_bytes, 0, lk * row_bytes, s));
+      if (st != ZL_OK) return st;
+    }
+  }
+  if (plan.tq == 0) return ZL_OK;
+
+  float* dq_acc = static_cast<float*>(workspace);
+  float* dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + dq_bytes);
+  st = launch_counted("bwd_preprocess", s, [&] {
+    return zl::launch_bwd_preprocess(head_dim, o, dout, dsum, dq_acc, plan.tq, num_heads, sms, s);
+  });
+  if (st != ZL_OK) return st;
+
+  // The backward of a split sequence is the sum over its tiles, which is the
+  // backward of the whole sequence: every sequence runs whole here, costed by
+  // the query blocks each of its key blocks visits, longest first.
+  struct BSeg {
+    zl::BwdSeg seg;
+    int64_t cost;
+  };
+  std::vector<BSeg> segs;
+  for (int32_t i = 0; i < num_seqs; ++i) {
+    const int32_t lq = cu_seqlens_q[i + 1] - cu_seqlens_q[i];
+    const int32_t lk = cu_seqlens_k[i + 1] - cu_seqlens_k[i];
+    if (lq == 0 || lk == 0) continue;
+    segs.push_back(BSeg{zl::BwdSeg{cu_seqlens_q[i], cu_seqlens_k[i], lq, lk, 0}, lq});
+  }
+  std::stable_sort(segs.begin(), segs.end(), [](const BSeg& a, const BSeg& c) { return a.cost > c.cost; });
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_map(&mq, q, plan.tq, num_heads, head_dim) || !make_map(&mk, k, plan.tk, num_heads, head_dim) ||
+      !make_map(&mv, v, plan.tk, num_heads, head_dim) || !make_map(&mdo, dout, plan.tq, num_heads, head_dim))
+    return ZL_ECUDA;
+  static thread_local zl::BwdArgs args;
+  std::memset(&args, 0, sizeof(args));
+  args.lse = lse;
+  args.dsum = dsum;
+  args.dq_acc = dq_acc;
+  args.dk = dk;
+  args.dv = dv;
+  args.lse_stride = plan.tq;
+  args.num_heads = num_heads;
+  args.scale = softmax_scale;
+  args.scale_log2 = softmax_scale * 1.4426950408889634f;
+  for (size_t first = 0; first < segs.size(); first += kMaxSegs) {
+    const size_t last = std::min(segs.size(), first + kMaxSegs);
+    int64_t items = 0;
+    args.n_segs = static_cast<int32_t>(last - first);
+    for (size_t i = first; i < last; ++i) {
+      zl::BwdSeg b = segs[i].seg;
+      b.item0 = static_cast<int32_t>(items);
+      args.segs[i - first] = b;
+      items += int64_t(num_heads) * ((b.k_len + kBlockN - 1) / kBlockN);
+    }
+    args.n_items = static_cast<int32_t>(items);
+    if (items == 0) continue;
+    const int grid = static_cast<int>(std::min<int64_t>(items, sms));
+    st = launch_counted("bwd_tc", s, [&] { return zl::launch_bwd_tc(head_dim, mq, mk, mv, mdo, args, grid, s); });
+    if (st != ZL_OK) return st;
+  }
+  return launch_counted("dq_convert", s, [&] {
+    return zl::launch_dq_convert(head_dim, dq_acc, dq, plan.tq, num_heads, softmax_scale, sms, s);
+  });
+}
+
+zl_status zl_profile_begin(void) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (g_prof_on) return ZL_EINVAL;
+  g_prof_on = true;
+  g_prof.clear();
+  return ZL_OK;
+}
+
+zl_status zl_profile_end(zl_profile_entry_t* entries, int32_t max_entries, int32_t* n_entries) {
+  std::vector<ProfRecord> recs;
+  {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    if (!g_prof_on) return ZL_EINVAL;
+    g_prof_on = false;
+    recs.swap(g_prof);
+  }
+  std::vector<zl_profile_entry_t> agg;
+  zl_status st = ZL_OK;
+  for (const ProfRecord& r : recs) {
+    float ms = 0.f;
+    if (st == ZL_OK &&
+        (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)) {
+      cudaGetLastError();
+      st = ZL_ECUDA;
+    }
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+    size_t i = 0;
+    while (i < agg.size() && std::strncmp(agg[i].name, r.name, sizeof(agg[i].name)) != 0) ++i;
+    if (i == agg.size()) {
+      zl_profile_entry_t e;
+      std::memset(&e, 0, sizeof(e));
+      std::strncpy(e.name, r.name, sizeof(e.name) - 1);
+      agg.push_back(e);
+    }
+    agg[i].launches += 1;
+    agg[i].total_ms += ms;
+  }
+  int32_t n = 0;
+  for (size_t i = 0; i < agg.size() && entries && n < max_entries; ++i) entries[n++] = agg[i];
+  if (n_entries) *n_entries = n;
+  return st;
 }
 
 zl_status zl_sync_check(void* stream) {
@@ -464,9 +639,10 @@ zl_status zl_sync_check(void* stream) {
     cudaGetLastError();
     return ZL_ECUDA;
   }
-  const uint32_t e = zl::fwd_take_error();
-  if (e == 0xFFFFFFFFu) return ZL_ECUDA;
-  if (e != 0) return ZL_ETIMEOUT;
+  const uint32_t ef = zl::fwd_take_error();
+  const uint32_t eb = zl::bwd_take_error();
+  if (ef == 0xFFFFFFFFu || eb == 0xFFFFFFFFu) return ZL_ECUDA;
+  if (ef != 0 || eb != 0) return ZL_ETIMEOUT;
   return ZL_OK;
 }
 

@@ -280,3 +280,30 @@ def dq_rows(q, k, v, do, cu_q, cu_k, seq, head, rows, scale=None):
     dp = dor @ vv.T
     dsum = (dor * o_r).sum(axis=1)
     return grad_q(grad_scores(p, dp, dsum), kk, scale)
+
+
+def dkdv_rows(q, k, v, do, cu_q, cu_k, seq, head, kv_rows, scale=None):
+    """dK and dV of selected key rows (relative to sequence `seq`) of one head.
+
+    A key row's gradients sum over every query row i of its sequence:
+      dV_j = sum_i P_ij dO_i,   dK_j = scale * sum_i P_ij (dO_i . v_j - D_i) q_i
+    so this first computes LSE and D = rowsum(dO * O) for all query rows (the
+    full forward of that head), then only the selected columns of P.
+    Returns (dk [len(kv_rows), d], dv [len(kv_rows), d])."""
+    d = q.shape[2]
+    if scale is None:
+        scale = default_scale(d)
+    qa, qb = int(cu_q[seq]), int(cu_q[seq + 1])
+    ka, kb = int(cu_k[seq]), int(cu_k[seq + 1])
+    kv_rows = np.asarray(kv_rows, dtype=np.int64)
+    qq, dd = q[qa:qb, head], do[qa:qb, head]
+    kk, vv = k[ka:kb, head], v[ka:kb, head]
+    o, lse = attention_f64(qq, kk, vv, scale)
+    dsum = (dd * o).sum(axis=1)
+    s_cols = scores(qq, kk[kv_rows], scale)                # [Lq, |J|]
+    p = probabilities(s_cols, lse)
+    dv = grad_v(p, dd)
+    dp = dd @ vv[kv_rows].T
+    ds = grad_scores(p, dp, dsum)
+    dk = grad_k(ds, qq, scale)
+    return dk, dv

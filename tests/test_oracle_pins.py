@@ -282,6 +282,10 @@ def pin_row_helpers():
     assert np.allclose(lrow, lse[1, 20 + np.array(rows)], atol=1e-13)
     dqr = oracle.dq_rows(q, k, v, do, cu, cu, 1, 0, rows)
     assert np.allclose(dqr, dq[20 + np.array(rows), 0], atol=1e-13)
+    _, dk, dv = oracle.varlen_attn_bwd(q, k, v, do, cu, cu)
+    dkr, dvr = oracle.dkdv_rows(q, k, v, do, cu, cu, 1, 1, rows)
+    assert np.allclose(dkr, dk[20 + np.array(rows), 1], atol=1e-12)
+    assert np.allclose(dvr, dv[20 + np.array(rows), 1], atol=1e-12)
 
 
 PINS = [pin_length_one, pin_constant_keys, pin_identical_values,

@@ -150,6 +150,20 @@ def gpu_index_for_smi(local_rank: int) -> str:
     return str(local_rank)
 
 
+def reduce_max_ms(ms_local: float, world: int, device) -> float:
+    """Slowest rank's time: the job is done when its last replica is."""
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, steps: int, flops_step: float, ms_max: float) -> float:
+    """Whole-job throughput: the work of every replica over the slowest time."""
+    return world * steps * flops_step / (ms_max * 1e-3) / 1e12
+
+
 def fwd_flops(wl) -> float:
     return 4.0 * wl.head_dim * wl.num_heads * wl.pair_count()
 
@@ -272,14 +286,10 @@ def main():
     clocks = sampler.stop()
     launches = zl.launch_count() - n_launch0
     zl.sync_check()
-    ms_local = e0.elapsed_time(e1)
-    ms = torch.tensor([ms_local], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
-    ms_total = float(ms.item())
+    ms_total = reduce_max_ms(e0.elapsed_time(e1), world, dev)
     flops_fwd = fwd_flops(wl)
     flops_step = flops_fwd * (3.5 if step_bwd else 1.0)
-    value = world * args.steps * flops_step / (ms_total * 1e-3) / 1e12
+    value = job_tflops(world, args.steps, flops_step, ms_total)
 
     # ---------------- per-kernel roofline of the dominant kernel
     dom = max(prof.items(), key=lambda kv: kv[1][1])[0] if prof else None
@@ -339,12 +349,10 @@ def main():
         f1.record()
         torch.cuda.synchronize()
         barrier()
-        ems = torch.tensor([f0.elapsed_time(f1)], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(ems, op=dist.ReduceOp.MAX)
+        ems = reduce_max_ms(f0.elapsed_time(f1), world, dev)
         bi = sum(t.numel() * t.element_size() for t in host_in.values())
         bo = sum(t.numel() * t.element_size() for t in host_out.values())
-        e2e = {"value": round(world * k_e2e * flops_step / (float(ems.item()) * 1e-3) / 1e12, 1),
+        e2e = {"value": round(job_tflops(world, k_e2e, flops_step, ems), 1),
                "unit": "TFLOP/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": k_e2e}
         del dev_in, host_in, host_out
 

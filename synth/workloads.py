@@ -108,6 +108,7 @@ def config(n: int) -> Workload:
        launch as 64 images of 1024 tokens; 40 heads, d = 128
     5  training step: one 720p 81-frame video as a 2 x 2 tile grid, two 480p
        81-frame videos, 4 images of 4096 and 32 of 1024 tokens; 40 heads
+    6  profiling case: one 480p 81-frame video (32,760 tokens), 24 heads
     """
     v480_81 = video_tokens(81, *RESOLUTIONS["480p"])     # 32,760
     v480_33 = video_tokens(33, *RESOLUTIONS["480p"])     # 14,040
@@ -128,6 +129,9 @@ def config(n: int) -> Workload:
         return Workload("train_step",
                         [v720_81] + [v480_81] * 2 + [img1024] * 4 + [img512] * 32, 40, 128,
                         splits={0: (2, 2)})
+    if n == 6:
+        # profiling case: one long video alone, fewer heads (inputs ~200 MB)
+        return Workload("video_32k_h24", [v480_81], 24, 128)
     raise ValueError(f"no workload {n}")
 
 

@@ -1,0 +1,51 @@
+"""Replica aggregation of bench.py across ranks, on CPU with gloo (world size
+2): the job time is the slowest rank's, the value counts every rank's work,
+and the reference arm runs on rank 0 only."""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms = bench.reduce_max_ms(100.0 + 50.0 * rank, world, torch.device("cpu"))
+    out[rank] = (ms, bench.job_tflops(world, 10, 1e15, ms))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_value():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    assert res[0][0] == res[1][0] == 150.0
+    # 2 replicas x 10 steps x 1 PFLOP in 150 ms
+    assert abs(res[0][1] - 2 * 10 * 1e15 / 0.150 / 1e12) < 1e-6
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], env=env, capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 0
+    assert r.stdout.strip() == ""

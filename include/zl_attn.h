@@ -193,6 +193,39 @@ zl_status zl_varlen_attn_bwd(
     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Backward that needs no workspace.  The paper has no counterpart to this
+ * entry point; it exists for callers that cannot allocate device memory at
+ * the moment they need a gradient: a plugin inside an engine that owns all
+ * device memory and forbids allocation while it executes, code between
+ * stream-capture begin and end, where a new allocation would not be part of
+ * the captured work, or a process whose memory a pooling allocator has
+ * reserved and that may not call it.
+ *
+ * Same operation, arguments and layouts as zl_varlen_attn_bwd with
+ * dtype = ZL_BF16, minus the tile table (tiles do not change a backward's
+ * result) and the workspace.  Its scratch (float32 dQ accumulator and D) is a
+ * 64 MiB array in the library's device image, reserved on every GPU the
+ * library is loaded on until the process exits.  Limit: Tq * H * d (rounded
+ * up to a multiple of 64) + Tq * H <= 16,777,216 float32 values, e.g.
+ * Tq <= 3,250 tokens at H = 40, d = 128; a larger batch returns
+ * ZL_EWORKSPACE before any GPU work.  The caller still owns and passes every
+ * input and output.
+ *
+ * The first call on each device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * All calls on a device share the array: calls whose kernels may overlap on
+ * the GPU (unordered streams) race on it and give undefined results; calls on
+ * one stream are safe.  Each call clears the accumulator it uses, so results
+ * do not depend on earlier calls.  Allocates no memory.
+ */
+zl_status zl_varlen_attn_bwd_static(
+    const void* q, const void* k, const void* v, const void* o, const float* lse,
+    const void* dout,
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
+    int32_t num_heads, int32_t head_dim, float softmax_scale,
+    void* dq, void* dk, void* dv, void* stream);
+
+/*
  * Synchronizes `stream`, then reports (and clears) any error a kernel of this
  * library flagged on the current device: ZL_ETIMEOUT when a bounded wait
  * inside a kernel ran out (the kernel stopped early and its outputs are

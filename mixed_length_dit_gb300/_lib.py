@@ -28,7 +28,7 @@ ZL_FP32 = 1
 EXPORTS = (
     "zl_status_string", "zl_version", "zl_varlen_attn_fwd_workspace_size", "zl_varlen_attn_fwd",
     "zl_lse_merge", "zl_varlen_attn_bwd_workspace_size", "zl_varlen_attn_bwd", "zl_sync_check",
-    "zl_launch_count", "zl_profile_begin", "zl_profile_end",
+    "zl_launch_count", "zl_profile_begin", "zl_profile_end", "zl_varlen_attn_bwd_static",
 )
 
 
@@ -89,6 +89,9 @@ def load() -> ctypes.CDLL:
     lib.zl_profile_begin.argtypes = []
     lib.zl_profile_end.restype = c_i32
     lib.zl_profile_end.argtypes = [ctypes.POINTER(ProfileEntry), c_i32, ctypes.POINTER(c_i32)]
+    lib.zl_varlen_attn_bwd_static.restype = c_i32
+    lib.zl_varlen_attn_bwd_static.argtypes = [vp, vp, vp, vp, vp, vp, i32p, i32p, c_i32, c_i32, c_i32,
+                                              c_f32, vp, vp, vp, vp]
     _lib = lib
     return lib
 

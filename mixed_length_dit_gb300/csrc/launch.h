@@ -98,6 +98,9 @@ cudaError_t launch_bwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap
 cudaError_t launch_dq_convert(int head_dim, const float* dq_acc, void* dq, int64_t tq,
                               int32_t num_heads, float scale, int num_sms, cudaStream_t stream);
 
+// Counts one kernel launch in the process-wide launch counter.
+void note_launch();
+
 // Shared-memory bytes a CTA of the tensor-core forward / backward requests.
 size_t fwd_tc_smem_bytes(int head_dim);
 size_t bwd_tc_smem_bytes(int head_dim);

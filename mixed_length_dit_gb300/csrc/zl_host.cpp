@@ -340,6 +340,10 @@ zl_status cuda_status(cudaError_t e) {
 
 }  // namespace
 
+namespace zl {
+void note_launch() { g_launches.fetch_add(1); }
+}  // namespace zl
+
 // =================================================================== C ABI
 extern "C" {
 

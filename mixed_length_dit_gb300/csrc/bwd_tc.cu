@@ -47,12 +47,13 @@ struct BwdSmem {
   uint8_t v[kBlockN * HD * 2];
   uint8_t q[kBwdStages][kBlockM * HD * 2];
   uint8_t dout[kBwdStages][kBlockM * HD * 2];
-  uint8_t ds[kBlockN * kBlockM * 2];              // dS^T rows: two 64-query halves
+  uint8_t ds[kBlockN * kBlockM * 2];              // dS^T rows (two 64-query halves), then dQ staging
   float lse2[kBlockM];                            // LSE * log2(e) of the query block
   float dsum[kBlockM];                            // D of the query block
   uint64_t kv_full, kv_empty;
   uint64_t qd_full[kBwdStages], qd_empty[kBwdStages];
   uint64_t s_full, sg_done, stage_full, dq_full, dq_drained, dkdv_full, dkdv_drained;
+  uint64_t dq_staged, dq_free;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -85,11 +86,21 @@ __device__ __forceinline__ void drain_delay(uint64_t ns) {
 // of the query block lives at [64h, 64h+32) of its region.
 __device__ __forceinline__ uint32_t op_col(int ks) { return (ks >> 2) * 64 + (ks & 3) * 8; }
 
+// The LSE*log2e (threads 0-127) or D (threads 128-255) value of query row t
+// of query block i; padding rows give P = 0 (LSE = +inf) and D = 0.
+__device__ __forceinline__ float staged_value(const BwdArgs& a, const BwdSeg& sg, int h, int i, int tid) {
+  const int t = tid & 127;
+  const int qg = i * kBlockM + t;
+  if (qg >= sg.q_len) return tid < 128 ? INFINITY : 0.f;
+  const size_t idx = static_cast<size_t>(h) * a.lse_stride + sg.q_row0 + qg;
+  return tid < 128 ? a.lse[idx] * kLog2e : a.dsum[idx];
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-              const __grid_constant__ BwdArgs args) {
+              const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ BwdArgs args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   auto* sm = reinterpret_cast<BwdSmem<HD>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -111,6 +122,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(&sm->dq_drained, kComputeThreads);
     mbar_init(&sm->dkdv_full, 1);
     mbar_init(&sm->dkdv_drained, kComputeThreads);
+    mbar_init(&sm->dq_staged, kComputeThreads);
+    mbar_init(&sm->dq_free, 1);
     sm->abort_flag = 0;
     fence_mbar_init();
   }
@@ -123,10 +136,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
   const uint32_t tS = tmem;          // S^T f32, then P^T bf16 at [64h, 64h+32)
-  const uint32_t tDP = tmem + 128;   // dP^T f32, then dS^T bf16 at 128 + [64h, 64h+32)
+  const uint32_t tDP = tmem + 128;   // dP^T f32, then dS^T bf16 at 128 + [64h, 64h+32), then dQ_i f32
   const uint32_t tDV = tmem + 256;
   const uint32_t tDK = tmem + 384;
-  const uint32_t tDQ = tmem;         // dQ_i f32 (after dV has read P^T)
+  const uint32_t tDQ = tDP;
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
@@ -181,31 +194,38 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const uint32_t ds_addr = smem_u32(sm->ds);
       uint32_t item_it = 0, qd_it = 0, blk = 0;
       bool ok = true;
+      // S^T = K Q_i^T into TMEM [0,128)
+      auto issue_s = [&](uint32_t st) {
+        const uint32_t q_addr = smem_u32(sm->q[st]);
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * (kBlockM * 128) + (ks & 3) * 32;
+          umma_ss(tS, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024), idesc_s,
+                  ks > 0 ? 1u : 0u);
+        }
+      };
       for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x, ++item_it) {
         const BwdWork w = decode_bwd(args, it);
         const BwdSeg& sg = args.segs[w.seg];
         const int nqb = (sg.q_len + kBlockM - 1) / kBlockM;
-        if (!mbar_wait(&sm->kv_full, item_it & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA)) {
+        if (!mbar_wait(&sm->kv_full, item_it & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA) ||
+            !mbar_wait(&sm->qd_full[qd_it % kBwdStages], (qd_it / kBwdStages) & 1u, abort_flag, &g_bwd_err,
+                       ERR_TIMEOUT_MMA)) {
           ok = false;
           break;
         }
+        tc_fence_after();
+        issue_s(qd_it % kBwdStages);
         for (int ii = 0; ii < nqb; ++ii, ++qd_it, ++blk) {
           const uint32_t st = qd_it % kBwdStages;
-          const uint32_t ph = (qd_it / kBwdStages) & 1u;
-          if (!mbar_wait(&sm->qd_full[st], ph, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA) ||
-              !mbar_wait(&sm->dq_drained, (blk & 1u) ^ 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA)) {
+          // dP^T = V dO_i^T into [128,256) once the previous dQ has been read out
+          if (!mbar_wait(&sm->dq_drained, (blk & 1u) ^ 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t q_addr = smem_u32(sm->q[st]);
           const uint32_t do_addr = smem_u32(sm->dout[st]);
-#pragma unroll
-          for (int ks = 0; ks < HD / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * (kBlockM * 128) + (ks & 3) * 32;
-            umma_ss(tS, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024), idesc_s,
-                    ks > 0 ? 1u : 0u);
-          }
 #pragma unroll
           for (int ks = 0; ks < HD / 16; ++ks) {
             const uint32_t off = (ks >> 2) * (kBlockM * 128) + (ks & 3) * 32;
@@ -231,6 +251,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             umma_ts(tDK, tDP + op_col(ks), sdesc_sw128(q_addr + ks * 2048, kBlockM * 128, 1024), idesc_acc,
                     (acc0 | (ks > 0 ? 1u : 0u)));
           }
+          // dQ_i = dS K into [128, 128+HD), after dK has read dS^T there
 #pragma unroll
           for (int ks = 0; ks < kBlockN / 16; ++ks) {
             umma_ss(tDQ, sdesc_sw128(ds_addr + ks * 2048, kBlockN * 128, 1024),
@@ -238,6 +259,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           }
           umma_commit(&sm->dq_full);
           umma_commit(&sm->qd_empty[st]);
+          if (ii + 1 < nqb) {
+            // next S^T overlaps the dQ drain (dV has read P^T out of [0,128))
+            const uint32_t nq = qd_it + 1;
+            if (!mbar_wait(&sm->qd_full[nq % kBwdStages], (nq / kBwdStages) & 1u, abort_flag, &g_bwd_err,
+                           ERR_TIMEOUT_MMA)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(nq % kBwdStages);
+          }
         }
         if (!ok) break;
         umma_commit(&sm->dkdv_full);
@@ -252,35 +284,29 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int jrow = w4 * 32 + lane;        // key row of S^T / dP^T, query row of dQ
     const int nh = args.num_heads;
     const float sl2 = args.scale_log2;
-    uint32_t item_it = 0, blk = 0;
-    for (int it = blockIdx.x; it < args.n_items; it += gridDim.x, ++item_it) {
+    uint32_t item_it = 0, blk = 0, stg = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x, ++item_it) {
       const BwdWork w = decode_bwd(args, it);
       const BwdSeg& sg = args.segs[w.seg];
       const int nqb = (sg.q_len + kBlockM - 1) / kBlockM;
       const int start = w.kb % nqb;
       const bool kv_ok = w.kb * kBlockN + jrow < sg.k_len;
-      bool ok = true;
+      float pref = staged_value(args, sg, w.h, start, threadIdx.x);
       for (int ii = 0; ii < nqb; ++ii, ++blk) {
         const int i = (start + ii) % nqb;
-        // Stage LSE*log2e and D of this query block (padding rows: P = 0,
-        // D = 0) once every compute thread is done with the previous block.
+        // Stage LSE*log2e and D of this query block once every compute
+        // thread is done with the previous one; prefetch the next block's.
         if (!__all_sync(0xffffffffu,
                         blk == 0 || mbar_wait(&sm->sg_done, (blk - 1) & 1u, abort_flag, &g_bwd_err,
                                               ERR_TIMEOUT_SOFTMAX))) {
           ok = false;
           break;
         }
-        {
-          const int t = threadIdx.x & 127;
-          const int qg = i * kBlockM + t;
-          const bool q_ok = qg < sg.q_len;
-          const size_t idx = static_cast<size_t>(w.h) * args.lse_stride + sg.q_row0 + qg;
-          if (threadIdx.x < 128)
-            sm->lse2[t] = q_ok ? args.lse[idx] * kLog2e : INFINITY;
-          else
-            sm->dsum[t] = q_ok ? args.dsum[idx] : 0.f;
-        }
+        if (threadIdx.x < 128) sm->lse2[threadIdx.x] = pref;
+        else sm->dsum[threadIdx.x - 128] = pref;
         mbar_arrive(&sm->stage_full);
+        if (ii + 1 < nqb) pref = staged_value(args, sg, w.h, (start + ii + 1) % nqb, threadIdx.x);
         if (!__all_sync(0xffffffffu,
                         mbar_wait(&sm->stage_full, blk & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_SOFTMAX)) ||
             !__all_sync(0xffffffffu,
@@ -328,30 +354,51 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tc_fence_before();
         mbar_arrive(&sm->sg_done);
         // ---------------------------------------------- drain dQ_i
+        // Read this thread's HD/2 columns of its query row out of TMEM (which
+        // frees the columns for the next dP^T), then push them through the
+        // dS buffer (128-byte swizzled boxes of 32 columns) into the float32
+        // accumulator with TMA reduce-add.  Padding rows carry exact zeros.
         if (!__all_sync(0xffffffffu,
                         mbar_wait(&sm->dq_full, blk & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_SOFTMAX))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const int q_local = i * kBlockM + jrow;
-        float* dq_dst = args.dq_acc + (static_cast<size_t>(sg.q_row0 + q_local) * nh + w.h) * HD + half * (HD / 2);
+        uint32_t g[HD / 64][32];
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c) {
-          uint32_t g[32];
-          tmem_ld32(tDQ + lane_off + half * (HD / 2) + 32 * c, g);
-          tmem_wait_ld();
-          reg_fence(g);
-          if (q_local < sg.q_len) {
+        for (int c = 0; c < HD / 64; ++c) tmem_ld32(tDQ + lane_off + half * (HD / 2) + 32 * c, g[c]);
+        tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              atomicAdd(reinterpret_cast<float4*>(dq_dst + 32 * c + 4 * e),
-                        make_float4(__uint_as_float(g[4 * e]), __uint_as_float(g[4 * e + 1]),
-                                    __uint_as_float(g[4 * e + 2]), __uint_as_float(g[4 * e + 3])));
-          }
-        }
+        for (int c = 0; c < HD / 64; ++c) reg_fence(g[c]);
         tc_fence_before();
         mbar_arrive(&sm->dq_drained);
+        uint8_t* box = sm->ds + half * (kBlockM * 128) + jrow * 128;
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c, ++stg) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            *reinterpret_cast<uint4*>(box + ((e ^ (jrow & 7)) << 4)) =
+                make_uint4(g[c][4 * e], g[c][4 * e + 1], g[c][4 * e + 2], g[c][4 * e + 3]);
+          fence_proxy_async_smem();
+          mbar_arrive(&sm->dq_staged);
+          if (threadIdx.x == 0) {
+            const bool staged = mbar_wait(&sm->dq_staged, stg & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_SOFTMAX);
+            if (staged) {
+              const int y = sg.q_row0 + i * kBlockM;
+              tma_reduce_add_2d(&tmDQ, sm->ds, w.h * HD + 32 * c, y);
+              tma_reduce_add_2d(&tmDQ, sm->ds + kBlockM * 128, w.h * HD + HD / 2 + 32 * c, y);
+              bulk_commit_group();
+              bulk_wait_group_read0();
+            }
+            mbar_arrive(&sm->dq_free);
+          }
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(&sm->dq_free, stg & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_SOFTMAX))) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
       }
       if (!ok) break;
       // ------------------------------------------------ dV, dK of the key block
@@ -391,6 +438,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       tc_fence_before();
       mbar_arrive(&sm->dkdv_drained);
     }
+    // the accumulator additions must have landed before the CTA exits
+    if (threadIdx.x == 0) bulk_wait_group0();
   }
 
   // ---------------------------------------------------------------- teardown
@@ -404,12 +453,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
 template <int HD>
 cudaError_t launch_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                      const CUtensorMap& tdo, const BwdArgs& args, int grid, cudaStream_t stream) {
+                      const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& args, int grid,
+                      cudaStream_t stream) {
   const size_t smem = sizeof(BwdSmem<HD>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  bwd_tc_kernel<HD><<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, args);
+  bwd_tc_kernel<HD><<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, args);
   return cudaGetLastError();
 }
 
@@ -420,10 +470,10 @@ size_t bwd_tc_smem_bytes(int head_dim) {
 }
 
 cudaError_t launch_bwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
-                          int grid, cudaStream_t stream) {
-  if (head_dim == 64) return launch_hd<64>(tq, tk, tv, tdo, args, grid, stream);
-  if (head_dim == 128) return launch_hd<128>(tq, tk, tv, tdo, args, grid, stream);
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                          const BwdArgs& args, int grid, cudaStream_t stream) {
+  if (head_dim == 64) return launch_hd<64>(tq, tk, tv, tdo, tdq, args, grid, stream);
+  if (head_dim == 128) return launch_hd<128>(tq, tk, tv, tdo, tdq, args, grid, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -92,9 +92,11 @@ cudaError_t launch_merge(int head_dim, const MergeArgs& args, int num_sms, cudaS
 cudaError_t launch_bwd_preprocess(int head_dim, const void* o, const void* dout, float* dsum,
                                   float* dq_acc, int64_t tq, int32_t num_heads, int num_sms,
                                   cudaStream_t stream);
+// tdq: float32 view [Tq][H*d] of the dQ accumulator, 32-column x 128-row
+// boxes with the 128-byte swizzle (the kernel adds into it with TMA).
 cudaError_t launch_bwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdArgs& args,
-                          int grid, cudaStream_t stream);
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                          const BwdArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_dq_convert(int head_dim, const float* dq_acc, void* dq, int64_t tq,
                               int32_t num_heads, float scale, int num_sms, cudaStream_t stream);
 

@@ -157,6 +157,20 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int nh, int hd) 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// float32 view [rows][H*d] of the dQ accumulator: boxes of 32 columns x 128
+// rows with the 128-byte swizzle, the shape the backward adds with TMA.
+bool make_map_acc(CUtensorMap* map, const float* base, int64_t rows, int nh, int hd) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nh) * hd, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nh) * hd * 4};
+  const cuuint32_t box[2] = {32, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ validation
 struct SplitSeq {
   int seq = 0;
@@ -558,9 +572,10 @@ zl_status zl_varlen_attn_bwd(const void* q, const void* k, const void* v, const 
     segs.push_back(BSeg{zl::BwdSeg{cu_seqlens_q[i], cu_seqlens_k[i], lq, lk, 0}, lq});
   }
   std::stable_sort(segs.begin(), segs.end(), [](const BSeg& a, const BSeg& c) { return a.cost > c.cost; });
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   if (!make_map(&mq, q, plan.tq, num_heads, head_dim) || !make_map(&mk, k, plan.tk, num_heads, head_dim) ||
-      !make_map(&mv, v, plan.tk, num_heads, head_dim) || !make_map(&mdo, dout, plan.tq, num_heads, head_dim))
+      !make_map(&mv, v, plan.tk, num_heads, head_dim) || !make_map(&mdo, dout, plan.tq, num_heads, head_dim) ||
+      !make_map_acc(&mdq, dq_acc, plan.tq, num_heads, head_dim))
     return ZL_ECUDA;
   static thread_local zl::BwdArgs args;
   std::memset(&args, 0, sizeof(args));
@@ -586,7 +601,7 @@ zl_status zl_varlen_attn_bwd(const void* q, const void* k, const void* v, const 
     args.n_items = static_cast<int32_t>(items);
     if (items == 0) continue;
     const int grid = static_cast<int>(std::min<int64_t>(items, sms));
-    st = launch_counted("bwd_tc", s, [&] { return zl::launch_bwd_tc(head_dim, mq, mk, mv, mdo, args, grid, s); });
+    st = launch_counted("bwd_tc", s, [&] { return zl::launch_bwd_tc(head_dim, mq, mk, mv, mdo, mdq, args, grid, s); });
     if (st != ZL_OK) return st;
   }
   return launch_counted("dq_convert", s, [&] {

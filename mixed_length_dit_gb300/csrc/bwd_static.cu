@@ -96,26 +96,26 @@ EncodeTiledFn static_encode_fn() {
   return fn;
 }
 
-bool static_map(CUtensorMap* map, const void* base, int64_t rows, int nh, int hd) {
+bool static_map(CUtensorMap* map, const void* base, int64_t rows, int nh, int hd, int box_rows = 128) {
   EncodeTiledFn fn = static_encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nh) * hd, static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nh) * hd * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// float32 view [rows][H*d] of the dQ accumulator: boxes of 32 columns x 128
-// rows with the 128-byte swizzle, the shape the backward adds with TMA.
-bool static_map_acc(CUtensorMap* map, const float* base, int64_t rows, int nh, int hd) {
+// float32 view [rows][H*d] of the dQ accumulator: boxes of 32 columns x
+// box_rows rows with the 128-byte swizzle, the shape the backward adds with TMA.
+bool static_map_acc(CUtensorMap* map, const float* base, int64_t rows, int nh, int hd, int box_rows) {
   EncodeTiledFn fn = static_encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nh) * hd, static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nh) * hd * 4};
-  const cuuint32_t box[2] = {32, 128};
+  const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -179,9 +179,10 @@ extern "C" zl_status zl_varlen_attn_bwd_static(
   }
   zl::note_launch();
   CUtensorMap mq, mk, mv, mdo, mdq;
-  if (!static_map(&mq, q, tq, num_heads, head_dim) || !static_map(&mk, k, tk, num_heads, head_dim) ||
-      !static_map(&mv, v, tk, num_heads, head_dim) || !static_map(&mdo, dout, tq, num_heads, head_dim) ||
-      !static_map_acc(&mdq, dq_acc, tq, num_heads, head_dim))
+  const int bq = zl::bwd_query_block();
+  if (!static_map(&mq, q, tq, num_heads, head_dim, bq) || !static_map(&mk, k, tk, num_heads, head_dim) ||
+      !static_map(&mv, v, tk, num_heads, head_dim) || !static_map(&mdo, dout, tq, num_heads, head_dim, bq) ||
+      !static_map_acc(&mdq, dq_acc, tq, num_heads, head_dim, bq))
     return ZL_ECUDA;
   static thread_local zl::BwdArgs args;
   args.lse = lse;

@@ -92,8 +92,13 @@ cudaError_t launch_merge(int head_dim, const MergeArgs& args, int num_sms, cudaS
 cudaError_t launch_bwd_preprocess(int head_dim, const void* o, const void* dout, float* dsum,
                                   float* dq_acc, int64_t tq, int32_t num_heads, int num_sms,
                                   cudaStream_t stream);
-// tdq: float32 view [Tq][H*d] of the dQ accumulator, 32-column x 128-row
-// boxes with the 128-byte swizzle (the kernel adds into it with TMA).
+// Query rows per block of the backward kernel: the row count of the Q / dO
+// tensor-map boxes and of the dQ accumulator boxes it is launched with.
+int bwd_query_block();
+// tq, tdo: bf16 maps with 64-column x bwd_query_block()-row boxes; tk, tv:
+// 64 x 128 boxes; tdq: float32 view [Tq][H*d] of the dQ accumulator with
+// 32-column x bwd_query_block()-row boxes, 128-byte swizzle (the kernel adds
+// into it with TMA).
 cudaError_t launch_bwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                           const BwdArgs& args, int grid, cudaStream_t stream);

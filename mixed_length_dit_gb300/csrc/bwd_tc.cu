@@ -20,16 +20,18 @@
 //     dK  += dS^T Q_i       (TS MMA)                   -> TMEM
 //     dQ_i^T = K_j^T dS_i^T (SS MMA, both MN-major)    -> S[b] (d on the lanes)
 //     drain warps read dQ_i^T out of TMEM, stage it in 128-byte-swizzled
-//       32-column boxes and add it into a float32 accumulator in global
-//       memory with TMA reduce-add; dq_convert later scales and rounds it.
+//       32-column boxes inside the now dead Q_i/dO_i stage, and add it into a
+//       float32 accumulator in global memory with TMA reduce-add; the stage is
+//       handed back to the producer once the copy engine has read it.
+//       dq_convert later scales and rounds the accumulator.
 // With two buffers the MMA warp issues (S^T, dP^T) for two query blocks, then
 // their (dV, dK, dQ) pair, so the softmax-grad of one block and the drain of
 // the previous overlap the tensor work of the other.
 //
 // Roles (448 threads, one CTA per SM): warps 0-7 softmax-grad (warp w reads
 // TMEM lanes 32*(w%4).. and query columns 32*(w/4)..) and the dV/dK epilogue,
-// warps 8-11 dQ drain, warp 12 TMA producer, warp 13 MMA issuer.  Every wait
-// is bounded.
+// warps 8-11 dQ drain, warp 12 TMA producer (4-stage Q/dO ring), warp 13 MMA
+// issuer.  Every wait is bounded.
 #include "common.cuh"
 #include "launch.h"
 
@@ -45,7 +47,7 @@ constexpr int kDrainThreads = 128;
 constexpr int kDrainWarp0 = 8;
 constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
-constexpr int kQdStages = 3;
+constexpr int kQdStages = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -53,10 +55,10 @@ template <int HD>
 struct BwdSmem {
   uint8_t k[kBlockN * HD * 2];                    // HD/64 boxes of [128 rows][128 B]
   uint8_t v[kBlockN * HD * 2];
-  uint8_t q[kQdStages][kBQ * HD * 2];             // HD/64 boxes of [64 rows][128 B]
-  uint8_t dout[kQdStages][kBQ * HD * 2];
+  // Q_i then dO_i, each HD/64 boxes of [64 rows][128 B]; after the block's
+  // MMAs, the dQ staging boxes ([64 rows][32 floats], one per drain warp)
+  uint8_t qd[kQdStages][2 * kBQ * HD * 2];
   uint8_t ds[2][kBlockN * kBQ * 2];               // dS as [128 key rows][64 queries], 128B-swizzled
-  uint8_t stage[4][kBQ * 128];                    // dQ staging: one [64 rows][32 floats] box per drain warp
   float lse2[2][kBQ];                             // LSE * log2(e) of the query block
   float dsum[2][kBQ];                             // D of the query block
   uint64_t kv_full, kv_empty;
@@ -123,7 +125,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(&sm->kv_empty, 1);
     for (int s = 0; s < kQdStages; ++s) {
       mbar_init(&sm->qd_full[s], 1);
-      mbar_init(&sm->qd_empty[s], 1);
+      mbar_init(&sm->qd_empty[s], kDrainThreads / 32);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm->s_full[b], 1);
@@ -184,8 +186,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           mbar_arrive_expect_tx(&sm->qd_full[st], 2 * kBQ * HD * 2);
 #pragma unroll
           for (int c = 0; c < HD / 64; ++c) {
-            tma_load_2d(sm->q[st] + c * kBQ * 128, &tmQ, &sm->qd_full[st], x0 + c * 64, sg.q_row0 + i * kBQ);
-            tma_load_2d(sm->dout[st] + c * kBQ * 128, &tmDO, &sm->qd_full[st], x0 + c * 64,
+            tma_load_2d(sm->qd[st] + c * kBQ * 128, &tmQ, &sm->qd_full[st], x0 + c * 64, sg.q_row0 + i * kBQ);
+            tma_load_2d(sm->qd[st] + kBQ * HD * 2 + c * kBQ * 128, &tmDO, &sm->qd_full[st], x0 + c * 64,
                         sg.q_row0 + i * kBQ);
           }
         }
@@ -221,8 +223,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               break;
             }
             tc_fence_after();
-            const uint32_t q_addr = smem_u32(sm->q[st]);
-            const uint32_t do_addr = smem_u32(sm->dout[st]);
+            const uint32_t q_addr = smem_u32(sm->qd[st]);
+            const uint32_t do_addr = q_addr + kBQ * HD * 2;
             const uint32_t tS = tmem + 64 * b;
             const uint32_t tDP = tmem + 128 + 64 * b;
 #pragma unroll
@@ -255,8 +257,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               break;
             }
             tc_fence_after();
-            const uint32_t q_addr = smem_u32(sm->q[st]);
-            const uint32_t do_addr = smem_u32(sm->dout[st]);
+            const uint32_t q_addr = smem_u32(sm->qd[st]);
+            const uint32_t do_addr = q_addr + kBQ * HD * 2;
             const uint32_t ds_addr = smem_u32(sm->ds[b]);
             const uint32_t tS = tmem + 64 * b;
             const uint32_t tDP = tmem + 128 + 64 * b;
@@ -279,7 +281,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                       sdesc_sw128(ds_addr + ks * 2048, 16, 1024), idesc_dq, ks > 0 ? 1u : 0u);
             }
             umma_commit(&sm->dq_full[b]);
-            umma_commit(&sm->qd_empty[st]);
           }
         }
         if (!ok) break;
@@ -293,9 +294,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int dw = warp - kDrainWarp0;                 // TMEM lane quadrant = d / 32
     const uint32_t lane_off = static_cast<uint32_t>(dw * 32) << 16;
     const bool active = dw * 32 < HD;
-    uint8_t* box = sm->stage[dw];
     uint32_t g = 0;
-    bool pending = false;
     bool ok = true;
     for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x) {
       const BwdWork w = decode_bwd(args, it);
@@ -319,11 +318,15 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         reg_fence(v1);
         tc_fence_before();
         mbar_arrive(&sm->dq_drained[b]);
-        if (!active) continue;
-        // the previous reduce of this warp's box must have read it
-        if (pending && lane == 0) bulk_wait_group_read0();
-        __syncwarp();
-        // box: [64 query rows][32 d floats], 16-byte chunk c of row r at c ^ (r & 7)
+        const uint32_t st = g % kQdStages;
+        if (!active) {
+          if (lane == 0) mbar_arrive(&sm->qd_empty[st]);
+          continue;
+        }
+        // This warp's box in the dead Q_i/dO_i stage (the block's MMAs have
+        // completed): [64 query rows][32 d floats], 16-byte chunk c of row r
+        // at c ^ (r & 7).
+        uint8_t* box = sm->qd[st] + dw * (kBQ * 128);
         const uint32_t cl = static_cast<uint32_t>(lane) >> 2;
         const uint32_t wl = (static_cast<uint32_t>(lane) & 3u) * 4;
 #pragma unroll
@@ -336,8 +339,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (lane == 0) {
           tma_reduce_add_2d(&tmDQ, box, w.h * HD + 32 * dw, sg.q_row0 + i * kBQ);
           bulk_commit_group();
+          bulk_wait_group_read0();           // box read: the stage may be refilled
+          mbar_arrive(&sm->qd_empty[st]);
         }
-        pending = true;
       }
     }
     if (lane == 0) bulk_wait_group0();

@@ -21,17 +21,22 @@
 //     dQ_i^T = K_j^T dS_i^T (SS MMA, both MN-major)    -> S[b] (d on the lanes)
 //     drain warps read dQ_i^T out of TMEM, stage it in 128-byte-swizzled
 //       32-column boxes inside the now dead Q_i/dO_i stage, and add it into a
-//       float32 accumulator in global memory with TMA reduce-add; the stage is
-//       handed back to the producer once the copy engine has read it.
+//       float32 accumulator in global memory with TMA reduce-add (a bulk copy
+//       holds no load/store slots while L2 performs the additions); the stage
+//       goes back to the producer once the copy engine has read it.
 //       dq_convert later scales and rounds the accumulator.
-// With two buffers the MMA warp issues (S^T, dP^T) for two query blocks, then
-// their (dV, dK, dQ) pair, so the softmax-grad of one block and the drain of
-// the previous overlap the tensor work of the other.
+// Each query block's MMAs come from three issuing threads in different warps
+// (one thread issues a tcgen05.mma only every ~70-95 cycles, and the N = 64
+// MMAs here take 32-64 cycles of tensor time each): A issues S^T and dV
+// (everything on S[b]), B issues dP^T and dK (everything on DP[b]), C issues
+// dQ^T once dV has read P^T out of S[b].  A and B issue their (S^T or dP^T)
+// for two query blocks and then the two accumulations, so the softmax-grad of
+// one block overlaps the tensor work of the other.
 //
-// Roles (448 threads, one CTA per SM): warps 0-7 softmax-grad (warp w reads
+// Roles (512 threads, one CTA per SM): warps 0-7 softmax-grad (warp w reads
 // TMEM lanes 32*(w%4).. and query columns 32*(w/4)..) and the dV/dK epilogue,
-// warps 8-11 dQ drain, warp 12 TMA producer (4-stage Q/dO ring), warp 13 MMA
-// issuer.  Every wait is bounded.
+// warps 8-11 dQ drain, warp 12 TMA producer (4-stage Q/dO ring), warps 13-15
+// MMA issuers.  Every wait is bounded.
 #include "common.cuh"
 #include "launch.h"
 
@@ -41,12 +46,14 @@ namespace {
 __device__ uint32_t g_bwd_err;
 
 constexpr int kBQ = 64;                     // query rows per block in the backward
-constexpr int kBwdThreads = 448;
+constexpr int kBwdThreads = 512;
 constexpr int kSgThreads = 256;
 constexpr int kDrainThreads = 128;
 constexpr int kDrainWarp0 = 8;
 constexpr int kProducerWarp = 12;
-constexpr int kMmaWarp = 13;
+constexpr int kMmaWarpA = 13;               // S^T, dV      (everything on S[b])
+constexpr int kMmaWarpB = 14;               // dP^T, dK     (everything on DP[b])
+constexpr int kMmaWarpC = 15;               // dQ^T         (into S[b] after dV)
 constexpr int kQdStages = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -55,15 +62,13 @@ template <int HD>
 struct BwdSmem {
   uint8_t k[kBlockN * HD * 2];                    // HD/64 boxes of [128 rows][128 B]
   uint8_t v[kBlockN * HD * 2];
-  // Q_i then dO_i, each HD/64 boxes of [64 rows][128 B]; after the block's
-  // MMAs, the dQ staging boxes ([64 rows][32 floats], one per drain warp)
-  uint8_t qd[kQdStages][2 * kBQ * HD * 2];
+  uint8_t qd[kQdStages][2 * kBQ * HD * 2];        // Q_i then dO_i, HD/64 boxes of [64 rows][128 B] each
   uint8_t ds[2][kBlockN * kBQ * 2];               // dS as [128 key rows][64 queries], 128B-swizzled
   float lse2[2][kBQ];                             // LSE * log2(e) of the query block
   float dsum[2][kBQ];                             // D of the query block
   uint64_t kv_full, kv_empty;
   uint64_t qd_full[kQdStages], qd_empty[kQdStages];
-  uint64_t s_full[2], sg_done[2], dq_full[2], dq_drained[2];
+  uint64_t s_full[2], sg_done[2], dv_done[2], dk_done[2], dq_full[2], dq_drained[2];
   uint64_t stage_full, dkdv_full, dkdv_drained;
   uint32_t tmem_base;
   int abort_flag;
@@ -122,24 +127,26 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
   if (threadIdx.x == 0) {
     mbar_init(&sm->kv_full, 1);
-    mbar_init(&sm->kv_empty, 1);
+    mbar_init(&sm->kv_empty, 3);                   // A, B and C are done with K/V
     for (int s = 0; s < kQdStages; ++s) {
       mbar_init(&sm->qd_full[s], 1);
-      mbar_init(&sm->qd_empty[s], kDrainThreads / 32);
+      mbar_init(&sm->qd_empty[s], kDrainThreads / 32);   // each drain warp, after its reduce read the stage
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm->s_full[b], 1);
+      mbar_init(&sm->s_full[b], 2);                // S^T from A, dP^T from B
       mbar_init(&sm->sg_done[b], kSgThreads);
+      mbar_init(&sm->dv_done[b], 1);
+      mbar_init(&sm->dk_done[b], 1);
       mbar_init(&sm->dq_full[b], 1);
       mbar_init(&sm->dq_drained[b], kDrainThreads);
     }
     mbar_init(&sm->stage_full, kSgThreads);
-    mbar_init(&sm->dkdv_full, 1);
+    mbar_init(&sm->dkdv_full, 2);
     mbar_init(&sm->dkdv_drained, kSgThreads);
     sm->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarpA) {
     tmem_alloc(&sm->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -193,13 +200,92 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarpA || warp == kMmaWarpB) {
+    // ------------------------------------------------------------ MMA issuers A and B
+    // A: S^T_i = K Q_i^T -> S[b], then dV += P^T dO_i (P^T read from S[b]).
+    // B: dP^T_i = V dO_i^T -> DP[b], then dK += dS^T Q_i (dS^T from DP[b]).
+    // Each issues (S^T or dP^T) for two query blocks, then the two
+    // accumulations, so softmax-grad of one block overlaps the MMAs of the other.
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(kBlockN, kBQ, false, false);   // S^T, dP^T: M128 N64
+      const bool is_a = warp == kMmaWarpA;
+      constexpr uint32_t idesc_s = idesc_bf16(kBlockN, kBQ, false, false);   // M128 N64
       constexpr uint32_t idesc_acc = idesc_bf16(kBlockN, HD, false, true);   // dV, dK
-      constexpr uint32_t idesc_dq = idesc_bf16(128, kBQ, true, true);        // dQ^T: M128 N64
+      const uint32_t a_op = smem_u32(is_a ? sm->k : sm->v);                   // K for S^T, V for dP^T
+      const uint32_t t_acc = is_a ? tDV : tDK;
+      const uint32_t err = ERR_TIMEOUT_MMA;
+      uint32_t item_it = 0, g = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x, ++item_it) {
+        const BwdWork w = decode_bwd(args, it);
+        const BwdSeg& sg = args.segs[w.seg];
+        const int nqb = (sg.q_len + kBQ - 1) / kBQ;
+        if (!mbar_wait(&sm->kv_full, item_it & 1u, abort_flag, &g_bwd_err, err)) {
+          ok = false;
+          break;
+        }
+        for (int i0 = 0; i0 < nqb && ok; i0 += 2) {
+          const int n_in = nqb - i0 < 2 ? nqb - i0 : 2;
+          for (int u = 0; u < n_in; ++u) {
+            const uint32_t gg = g + i0 + u;
+            const uint32_t b = gg & 1u;
+            const uint32_t st = gg % kQdStages;
+            // A must also wait until dQ^T of block gg-2 has left S[b]
+            if (!mbar_wait(&sm->qd_full[st], (gg / kQdStages) & 1u, abort_flag, &g_bwd_err, err) ||
+                (is_a && !mbar_wait(&sm->dq_drained[b], ((gg >> 1) & 1u) ^ 1u, abort_flag, &g_bwd_err, err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // B operand: Q_i for S^T, dO_i for dP^T
+            const uint32_t b_op = smem_u32(sm->qd[st]) + (is_a ? 0u : static_cast<uint32_t>(kBQ * HD * 2));
+            const uint32_t t_out = tmem + (is_a ? 0u : 128u) + 64u * b;
+#pragma unroll
+            for (int ks = 0; ks < HD / 16; ++ks) {
+              const uint32_t ka = (ks >> 2) * (kBlockN * 128) + (ks & 3) * 32;
+              const uint32_t qa = (ks >> 2) * (kBQ * 128) + (ks & 3) * 32;
+              umma_ss(t_out, sdesc_sw128(a_op + ka, 16, 1024), sdesc_sw128(b_op + qa, 16, 1024), idesc_s,
+                      ks > 0 ? 1u : 0u);
+            }
+            umma_commit(&sm->s_full[b]);
+          }
+          if (!ok) break;
+          for (int u = 0; u < n_in; ++u) {
+            const int ii = i0 + u;
+            const uint32_t gg = g + ii;
+            const uint32_t b = gg & 1u;
+            const uint32_t st = gg % kQdStages;
+            if (!mbar_wait(&sm->sg_done[b], (gg >> 1) & 1u, abort_flag, &g_bwd_err, err) ||
+                (ii == 0 && !mbar_wait(&sm->dkdv_drained, (item_it & 1u) ^ 1u, abort_flag, &g_bwd_err, err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // dV: B = dO_i (MN-major); dK: B = Q_i (MN-major)
+            const uint32_t b_op = smem_u32(sm->qd[st]) + (is_a ? static_cast<uint32_t>(kBQ * HD * 2) : 0u);
+            const uint32_t t_a = tmem + (is_a ? 0u : 128u) + 64u * b;
+            const uint32_t acc0 = ii > 0 ? 1u : 0u;
+#pragma unroll
+            for (int ks = 0; ks < kBQ / 16; ++ks) {
+              umma_ts(t_acc, t_a + op_col(ks), sdesc_sw128(b_op + ks * 2048, kBQ * 128, 1024), idesc_acc,
+                      acc0 | (ks > 0 ? 1u : 0u));
+            }
+            umma_commit(is_a ? &sm->dv_done[b] : &sm->dk_done[b]);
+          }
+        }
+        if (!ok) break;
+        g += nqb;
+        umma_commit(&sm->dkdv_full);
+        umma_commit(&sm->kv_empty);
+      }
+    }
+  } else if (warp == kMmaWarpC) {
+    // ------------------------------------------------------------ MMA issuer C
+    // dQ_i^T = K^T dS_i^T into S[b] once dV has read P^T out of it.  A = K as
+    // MN-major (d on M; for d = 64 the upper 64 rows read the V tile and are
+    // never drained), B = dS MN-major.
+    if (lane == 0) {
+      constexpr uint32_t idesc_dq = idesc_bf16(128, kBQ, true, true);        // M128 N64
       const uint32_t k_addr = smem_u32(sm->k);
-      const uint32_t v_addr = smem_u32(sm->v);
       uint32_t item_it = 0, g = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x, ++item_it) {
@@ -210,87 +296,32 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           ok = false;
           break;
         }
-        for (int i0 = 0; i0 < nqb && ok; i0 += 2) {
-          const int n_in = nqb - i0 < 2 ? nqb - i0 : 2;
-          // (S^T, dP^T) of the pair
-          for (int u = 0; u < n_in; ++u) {
-            const uint32_t gg = g + i0 + u;
-            const uint32_t b = gg & 1u;
-            const uint32_t st = gg % kQdStages;
-            if (!mbar_wait(&sm->qd_full[st], (gg / kQdStages) & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA) ||
-                !mbar_wait(&sm->dq_drained[b], ((gg >> 1) & 1u) ^ 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t q_addr = smem_u32(sm->qd[st]);
-            const uint32_t do_addr = q_addr + kBQ * HD * 2;
-            const uint32_t tS = tmem + 64 * b;
-            const uint32_t tDP = tmem + 128 + 64 * b;
-#pragma unroll
-            for (int ks = 0; ks < HD / 16; ++ks) {
-              const uint32_t ka = (ks >> 2) * (kBlockN * 128) + (ks & 3) * 32;
-              const uint32_t qa = (ks >> 2) * (kBQ * 128) + (ks & 3) * 32;
-              umma_ss(tS, sdesc_sw128(k_addr + ka, 16, 1024), sdesc_sw128(q_addr + qa, 16, 1024), idesc_s,
-                      ks > 0 ? 1u : 0u);
-            }
-#pragma unroll
-            for (int ks = 0; ks < HD / 16; ++ks) {
-              const uint32_t ka = (ks >> 2) * (kBlockN * 128) + (ks & 3) * 32;
-              const uint32_t qa = (ks >> 2) * (kBQ * 128) + (ks & 3) * 32;
-              umma_ss(tDP, sdesc_sw128(v_addr + ka, 16, 1024), sdesc_sw128(do_addr + qa, 16, 1024), idesc_s,
-                      ks > 0 ? 1u : 0u);
-            }
-            umma_commit(&sm->s_full[b]);
+        for (int ii = 0; ii < nqb; ++ii) {
+          const uint32_t gg = g + ii;
+          const uint32_t b = gg & 1u;
+          if (!mbar_wait(&sm->sg_done[b], (gg >> 1) & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA) ||
+              !mbar_wait(&sm->dv_done[b], (gg >> 1) & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA)) {
+            ok = false;
+            break;
           }
-          if (!ok) break;
-          // (dV, dK, dQ^T) of the pair
-          for (int u = 0; u < n_in; ++u) {
-            const int ii = i0 + u;
-            const uint32_t gg = g + ii;
-            const uint32_t b = gg & 1u;
-            const uint32_t st = gg % kQdStages;
-            if (!mbar_wait(&sm->sg_done[b], (gg >> 1) & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA) ||
-                (ii == 0 &&
-                 !mbar_wait(&sm->dkdv_drained, (item_it & 1u) ^ 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t q_addr = smem_u32(sm->qd[st]);
-            const uint32_t do_addr = q_addr + kBQ * HD * 2;
-            const uint32_t ds_addr = smem_u32(sm->ds[b]);
-            const uint32_t tS = tmem + 64 * b;
-            const uint32_t tDP = tmem + 128 + 64 * b;
-            const uint32_t acc0 = ii > 0 ? 1u : 0u;
+          tc_fence_after();
+          const uint32_t ds_addr = smem_u32(sm->ds[b]);
 #pragma unroll
-            for (int ks = 0; ks < kBQ / 16; ++ks) {
-              umma_ts(tDV, tS + op_col(ks), sdesc_sw128(do_addr + ks * 2048, kBQ * 128, 1024), idesc_acc,
-                      acc0 | (ks > 0 ? 1u : 0u));
-            }
-#pragma unroll
-            for (int ks = 0; ks < kBQ / 16; ++ks) {
-              umma_ts(tDK, tDP + op_col(ks), sdesc_sw128(q_addr + ks * 2048, kBQ * 128, 1024), idesc_acc,
-                      acc0 | (ks > 0 ? 1u : 0u));
-            }
-            // dQ_i^T = K^T dS^T: A = K as MN-major (d on M; for d = 64 the upper
-            // 64 rows read the V tile and are never drained), B = dS MN-major.
-#pragma unroll
-            for (int ks = 0; ks < kBlockN / 16; ++ks) {
-              umma_ss(tS, sdesc_sw128(k_addr + ks * 2048, kBlockN * 128, 1024),
-                      sdesc_sw128(ds_addr + ks * 2048, 16, 1024), idesc_dq, ks > 0 ? 1u : 0u);
-            }
-            umma_commit(&sm->dq_full[b]);
+          for (int ks = 0; ks < kBlockN / 16; ++ks) {
+            umma_ss(tmem + 64 * b, sdesc_sw128(k_addr + ks * 2048, kBlockN * 128, 1024),
+                    sdesc_sw128(ds_addr + ks * 2048, 16, 1024), idesc_dq, ks > 0 ? 1u : 0u);
           }
+          umma_commit(&sm->dq_full[b]);
         }
         if (!ok) break;
         g += nqb;
-        umma_commit(&sm->dkdv_full);
         umma_commit(&sm->kv_empty);
       }
     }
   } else if (warp >= kDrainWarp0) {
     // ------------------------------------------------------------ dQ drain
+    // Lane l of drain warp dw holds dQ^T row d = 32 dw + l for the block's 64
+    // queries.  Rows past the sequence carry exact zeros (P = 0 there).
     const int dw = warp - kDrainWarp0;                 // TMEM lane quadrant = d / 32
     const uint32_t lane_off = static_cast<uint32_t>(dw * 32) << 16;
     const bool active = dw * 32 < HD;
@@ -323,9 +354,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           if (lane == 0) mbar_arrive(&sm->qd_empty[st]);
           continue;
         }
-        // This warp's box in the dead Q_i/dO_i stage (the block's MMAs have
-        // completed): [64 query rows][32 d floats], 16-byte chunk c of row r
-        // at c ^ (r & 7).
+        // dK (issuer B) may still be reading Q_i out of this stage
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&sm->dk_done[b], (g >> 1) & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_OTHER))) {
+          ok = false;
+          break;
+        }
+        // This warp's box in the dead Q_i/dO_i stage: [64 query rows][32 d
+        // floats], 16-byte chunk c of row r at c ^ (r & 7).
         uint8_t* box = sm->qd[st] + dw * (kBQ * 128);
         const uint32_t cl = static_cast<uint32_t>(lane) >> 2;
         const uint32_t wl = (static_cast<uint32_t>(lane) & 3u) * 4;
@@ -344,7 +380,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
       }
     }
-    if (lane == 0) bulk_wait_group0();
+    if (lane == 0) bulk_wait_group0();        // the additions must land before exit
   } else {
     // ------------------------------------------------------------ softmax-grad
     const int w4 = warp & 3;
@@ -466,7 +502,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarpA) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int HD>

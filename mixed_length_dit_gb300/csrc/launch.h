@@ -98,7 +98,7 @@ int bwd_query_block();
 // tq, tdo: bf16 maps with 64-column x bwd_query_block()-row boxes; tk, tv:
 // 64 x 128 boxes; tdq: float32 view [Tq][H*d] of the dQ accumulator with
 // 32-column x bwd_query_block()-row boxes, 128-byte swizzle (the kernel adds
-// into it with TMA).
+// into it with TMA).  args.dq_acc must be zeroed before the launch.
 cudaError_t launch_bwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                           const BwdArgs& args, int grid, cudaStream_t stream);

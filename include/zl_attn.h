@@ -119,8 +119,8 @@ zl_status zl_varlen_attn_fwd_workspace_size(
  * Whole sequences and every tile run in one persistent launch whose work
  * items (sequence-or-tile x head x 128-query block) are ordered longest
  * first, ties in input order.  Tiles write float32 partials into the
- * workspace, and one merge launch (zl_lse_merge's kernel) then combines each
- * query row's partials into o and lse exactly.  A sequence with queries but no
+ * workspace, and a merge launch per split sequence (zl_lse_merge's kernel)
+ * then combines each query row's partials into o and lse exactly.  A sequence with queries but no
  * keys is rejected (ZL_EINVAL); zero-length sequences are skipped.
  */
 zl_status zl_varlen_attn_fwd(
@@ -130,6 +130,30 @@ zl_status zl_varlen_attn_fwd(
     const zl_tile_t* tiles, int32_t num_tiles,
     void* o, float* lse,
     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Flags of zl_varlen_attn_fwd_ex. */
+enum {
+  /* Merge the tile partials inside the forward launch: each tile counts
+   * itself per (128-query block, head) after writing its partial, and the
+   * tile that completes the set merges the partials of those rows (exact, as
+   * zl_lse_merge; no waiting).  Saves the merge launch; measured slower than
+   * the separate merge on the long-video batches, because the merging CTA's
+   * tensor pipeline idles meanwhile.  bf16 only (ignored for ZL_FP32). */
+  ZL_FWD_FUSED_MERGE = 1
+};
+
+/*
+ * zl_varlen_attn_fwd with option flags (a bitwise OR of ZL_FWD_* values; 0
+ * gives exactly zl_varlen_attn_fwd).  Same arguments, layouts and workspace
+ * otherwise.
+ */
+zl_status zl_varlen_attn_fwd_ex(
+    const void* q, const void* k, const void* v,
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
+    int32_t num_heads, int32_t head_dim, int32_t dtype, float softmax_scale,
+    const zl_tile_t* tiles, int32_t num_tiles,
+    void* o, float* lse,
+    void* workspace, size_t workspace_bytes, void* stream, uint32_t flags);
 
 /*
  * Exact merge of partial attention results over disjoint key sets: the

@@ -29,7 +29,10 @@ EXPORTS = (
     "zl_status_string", "zl_version", "zl_varlen_attn_fwd_workspace_size", "zl_varlen_attn_fwd",
     "zl_lse_merge", "zl_varlen_attn_bwd_workspace_size", "zl_varlen_attn_bwd", "zl_sync_check",
     "zl_launch_count", "zl_profile_begin", "zl_profile_end", "zl_varlen_attn_bwd_static",
+    "zl_varlen_attn_fwd_ex",
 )
+
+ZL_FWD_FUSED_MERGE = 1
 
 
 class Tile(ctypes.Structure):
@@ -78,6 +81,9 @@ def load() -> ctypes.CDLL:
     lib.zl_varlen_attn_fwd.restype = c_i32
     lib.zl_varlen_attn_fwd.argtypes = [vp, vp, vp, i32p, i32p, c_i32, c_i32, c_i32, c_i32, c_f32,
                                        tilep, c_i32, vp, vp, vp, c_sz, vp]
+    lib.zl_varlen_attn_fwd_ex.restype = c_i32
+    lib.zl_varlen_attn_fwd_ex.argtypes = [vp, vp, vp, i32p, i32p, c_i32, c_i32, c_i32, c_i32, c_f32,
+                                          tilep, c_i32, vp, vp, vp, c_sz, vp, ctypes.c_uint32]
     lib.zl_lse_merge.restype = c_i32
     lib.zl_lse_merge.argtypes = [vp, vp, c_i32, c_i64, c_i32, c_i32, c_i64, vp, c_i32, vp, c_i64, vp]
     lib.zl_varlen_attn_bwd_workspace_size.restype = c_i32

@@ -68,8 +68,10 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor | None:
 
 
 def varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k=None, tiles=None, softmax_scale=None,
-                    out=None, lse=None, workspace=None, stream=None):
-    """Coalesced block-diagonal attention forward.  Returns (o, lse)."""
+                    out=None, lse=None, workspace=None, stream=None, fused_merge=False):
+    """Coalesced block-diagonal attention forward.  Returns (o, lse).
+    fused_merge merges tile partials inside the forward launch
+    (ZL_FWD_FUSED_MERGE)."""
     lib = _lib.load()
     if cu_seqlens_k is None:
         cu_seqlens_k = cu_seqlens_q
@@ -89,9 +91,10 @@ def varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k=None, tiles=None, softma
         raise ValueError("cu_seqlens_q and cu_seqlens_k differ in length")
     ta, nt = _lib.tile_array(tiles)
     ws_bytes = workspace.numel() if workspace is not None else 0
-    st = lib.zl_varlen_attn_fwd(_ptr(q), _ptr(k), _ptr(v), cq, ck, nq - 1, nh, hd, _dtype_code(q),
-                                scale, ta, nt, _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
-                                _stream_handle(stream))
+    flags = _lib.ZL_FWD_FUSED_MERGE if fused_merge else 0
+    st = lib.zl_varlen_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), cq, ck, nq - 1, nh, hd, _dtype_code(q),
+                                   scale, ta, nt, _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                                   _stream_handle(stream), flags)
     _lib.check(st, "zl_varlen_attn_fwd")
     return out, lse
 

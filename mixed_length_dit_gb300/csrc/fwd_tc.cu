@@ -21,8 +21,12 @@
 //              After the last block it normalises O and writes O and LSE.
 // TMEM: S/P in columns [0,128), O in [128, 128+d); 256 columns per CTA.
 //
-// Whole sequences write O in bf16 and LSE in natural log; tiles write float32
-// partial O and their own LSE into a partial slot for the merge kernel.
+// Whole sequences write O in bf16 and LSE in natural log.  Tiles write float32
+// partial O and their own LSE into a partial slot for the merge kernel; with
+// the fused merge they then count themselves in an arrival counter per
+// (query block, head) of their query chunk, and the CTA that brings the count
+// to the number of kv chunks merges all partials of those 128 rows into O and
+// LSE exactly (no waiting: every other partial is complete and fenced by then).
 #include "common.cuh"
 #include "launch.h"
 #include "work.cuh"
@@ -49,7 +53,50 @@ struct FwdSmem {
   uint64_t s_full, p_full, o_full;
   uint32_t tmem_base;
   int abort_flag;
+  int is_last;                                 // this CTA completed a tile row block's partials
 };
+
+// Merges the n_kv float32 partials of one query row of a tile (all written
+// and fenced by their CTAs) into the bf16 output and the LSE:
+//     lse = log sum_j exp(lse_j),  o = sum_j exp(lse_j - lse) o_j.
+template <int HD>
+__device__ __forceinline__ void merge_tile_row(const FwdArgs& a, const FwdSeg& sg, int h, int q_local) {
+  const int64_t nh = a.num_heads;
+  const size_t prow = static_cast<size_t>(sg.out_row0 + q_local);
+  float m = -INFINITY;
+  for (int j = 0; j < sg.n_kv; ++j)
+    m = fmaxf(m, __ldcg(a.lse_part + (static_cast<size_t>(j) * nh + h) * a.part_rows + prow));
+  float sum = 0.f;
+  for (int j = 0; j < sg.n_kv; ++j)
+    sum += expf(__ldcg(a.lse_part + (static_cast<size_t>(j) * nh + h) * a.part_rows + prow) - m);
+  const float inv = 1.f / sum;
+  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.o) + (static_cast<size_t>(sg.q_row0 + q_local) * nh + h) * HD;
+#pragma unroll 1
+  for (int c = 0; c < HD / 32; ++c) {
+    float acc[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+    for (int j = 0; j < sg.n_kv; ++j) {
+      const float wj = expf(__ldcg(a.lse_part + (static_cast<size_t>(j) * nh + h) * a.part_rows + prow) - m) * inv;
+      const float4* src = reinterpret_cast<const float4*>(
+          a.o_part + ((static_cast<size_t>(j) * a.part_rows + prow) * nh + h) * HD + c * 32);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 x = __ldcg(src + v);
+        acc[4 * v + 0] = fmaf(wj, x.x, acc[4 * v + 0]);
+        acc[4 * v + 1] = fmaf(wj, x.y, acc[4 * v + 1]);
+        acc[4 * v + 2] = fmaf(wj, x.z, acc[4 * v + 2]);
+        acc[4 * v + 3] = fmaf(wj, x.w, acc[4 * v + 3]);
+      }
+    }
+    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+      d4[v] = make_uint4(pack_bf16x2(acc[8 * v + 0], acc[8 * v + 1]), pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]),
+                         pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]), pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]));
+  }
+  a.lse[static_cast<size_t>(h) * a.lse_stride + sg.q_row0 + q_local] = m + logf(sum);
+}
 
 // Spin for about `ns` nanoseconds: lets copies and MMAs already in flight land
 // before an aborting CTA releases its shared memory and TMEM.
@@ -333,6 +380,18 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (row_ok)
           args.lse_part[(static_cast<size_t>(sg.slot) * nh + w.h) * args.part_rows + sg.out_row0 + q_local] =
               lse_val;
+        // Fused merge: publish this partial; the CTA that completes the set
+        // of kv chunks of this (query block, head) merges them into o / lse.
+        if (!args.fused_merge) continue;
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (row == 0)
+          sm->is_last = atomicAdd(args.counters + sg.counter0 + w.qb * nh + w.h, 1) == sg.n_kv - 1;
+        named_bar_sync(1, 128);
+        if (sm->is_last) {
+          __threadfence();
+          if (row_ok) merge_tile_row<HD>(args, sg, w.h, q_local);
+        }
       }
     }
   }

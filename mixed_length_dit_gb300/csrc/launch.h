@@ -13,7 +13,7 @@ constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 
 // Work segments passed by value in one launch (kernel parameter space).
-constexpr int kMaxSegs = 960;
+constexpr int kMaxSegs = 640;
 
 // One segment of forward work: a whole sequence or one shard tile.  Its work
 // items are (head, 128-row query block) pairs, numbered from item0 with the
@@ -26,6 +26,8 @@ struct FwdSeg {
   int32_t out_row0;  // whole: = q_row0 (row in o/lse); tile: row in the partial slot
   int32_t slot;      // -1: whole sequence, else the partial slot (kv chunk)
   int32_t item0;     // first work item of the segment
+  int32_t counter0;  // tile: first arrival counter of its query chunk (+ qb * H + h)
+  int32_t n_kv;      // tile: kv chunks of its sequence (partials to merge)
 };
 
 struct FwdArgs {
@@ -33,6 +35,8 @@ struct FwdArgs {
   float* lse;           // [H][lse_stride]
   float* o_part;        // partial O  [P][part_rows][H][d] f32
   float* lse_part;      // partial LSE [P][H][part_rows] f32
+  int32_t* counters;    // tile arrival counters, zero at launch (fused merge)
+  int32_t fused_merge;  // tensor-core path: the last arriving tile merges the partials
   int64_t lse_stride;   // Tq
   int64_t part_rows;    // R
   int32_t num_heads;

@@ -186,6 +186,7 @@ struct Plan {
   std::vector<zl_tile_t> tiles;     // sorted by (seq, q_chunk, kv_chunk)
   int64_t part_rows = 0;            // R
   int n_parts = 0;                  // P
+  int64_t n_counters = 0;           // arrival counters: (query chunk, 128-row block) x head
 };
 
 constexpr int64_t kMaxTokens = (int64_t(1) << 31) - 1 - 2 * kBlockM;
@@ -266,6 +267,10 @@ zl_status make_plan(const int32_t* cu_q, const int32_t* cu_k, int32_t b, int32_t
       q_expect += first.q_len;
     }
     if (q_expect != lq) return ZL_EINVAL;
+    for (int qc = 0; qc < n_q; ++qc) {
+      const zl_tile_t& first = plan->tiles[i + static_cast<size_t>(qc) * n_kv];
+      plan->n_counters += (first.q_len + kBlockM - 1) / kBlockM;   // times H below
+    }
     SplitSeq sp;
     sp.seq = seq;
     sp.n_kv = n_kv;
@@ -278,6 +283,7 @@ zl_status make_plan(const int32_t* cu_q, const int32_t* cu_k, int32_t b, int32_t
     i = j;
   }
   plan->part_rows = rbase;
+  plan->n_counters *= nh;
   return ZL_OK;
 }
 
@@ -287,7 +293,8 @@ size_t fwd_workspace_bytes(const Plan& p, int nh, int hd) {
   if (p.splits.empty()) return 0;
   const size_t o_bytes = static_cast<size_t>(p.n_parts) * p.part_rows * nh * hd * sizeof(float);
   const size_t l_bytes = static_cast<size_t>(p.n_parts) * nh * p.part_rows * sizeof(float);
-  return align256(o_bytes) + align256(l_bytes);
+  const size_t c_bytes = static_cast<size_t>(p.n_counters) * sizeof(int32_t);
+  return align256(o_bytes) + align256(l_bytes) + align256(c_bytes);
 }
 
 // ------------------------------------------------------------------ scheduler
@@ -298,8 +305,9 @@ struct Segment {
 };
 
 // Whole sequences and tiles as segments, stably ordered by decreasing cost.
-std::vector<Segment> schedule_fwd(const Plan& p, const int32_t* cu_q, const int32_t* cu_k, int32_t b) {
+std::vector<Segment> schedule_fwd(const Plan& p, const int32_t* cu_q, const int32_t* cu_k, int32_t b, int nh) {
   std::vector<Segment> segs;
+  int64_t counter_base = 0, counter_next = 0;   // arrival counters of the query chunks, in tile order
   segs.reserve(static_cast<size_t>(b) + p.tiles.size());
   size_t ti = 0;
   int order = 0;
@@ -310,7 +318,7 @@ std::vector<Segment> schedule_fwd(const Plan& p, const int32_t* cu_q, const int3
     if (si < 0) {
       if (lq == 0) continue;
       Segment g;
-      g.seg = FwdSeg{cu_q[s], cu_k[s], lq, lk, cu_q[s], -1, 0};
+      g.seg = FwdSeg{cu_q[s], cu_k[s], lq, lk, cu_q[s], -1, 0, 0, 0};
       g.cost = lk;
       g.order = order++;
       segs.push_back(g);
@@ -319,9 +327,14 @@ std::vector<Segment> schedule_fwd(const Plan& p, const int32_t* cu_q, const int3
       while (ti < p.tiles.size() && p.tiles[ti].seq < s) ++ti;
       for (; ti < p.tiles.size() && p.tiles[ti].seq == s; ++ti) {
         const zl_tile_t& t = p.tiles[ti];
+        if (t.kv_chunk == 0) {               // first tile of a new query chunk
+          counter_base += counter_next;
+          counter_next = static_cast<int64_t>((t.q_len + kBlockM - 1) / kBlockM) * nh;
+        }
         Segment g;
         g.seg = FwdSeg{cu_q[s] + t.q_start, cu_k[s] + t.k_start, t.q_len, t.k_len,
-                       static_cast<int32_t>(sp.rbase + t.q_start), t.kv_chunk, 0};
+                       static_cast<int32_t>(sp.rbase + t.q_start), t.kv_chunk, 0,
+                       static_cast<int32_t>(counter_base), sp.n_kv};
         g.cost = t.k_len;
         g.order = order++;
         segs.push_back(g);
@@ -426,6 +439,17 @@ zl_status zl_varlen_attn_fwd(const void* q, const void* k, const void* v, const 
                              int32_t head_dim, int32_t dtype, float softmax_scale, const zl_tile_t* tiles,
                              int32_t num_tiles, void* o, float* lse, void* workspace,
                              size_t workspace_bytes, void* stream) {
+  return zl_varlen_attn_fwd_ex(q, k, v, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, dtype,
+                               softmax_scale, tiles, num_tiles, o, lse, workspace, workspace_bytes, stream, 0u);
+}
+
+zl_status zl_varlen_attn_fwd_ex(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                                const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t num_heads,
+                                int32_t head_dim, int32_t dtype, float softmax_scale, const zl_tile_t* tiles,
+                                int32_t num_tiles, void* o, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream, uint32_t flags) {
+  if ((flags & ~static_cast<uint32_t>(ZL_FWD_FUSED_MERGE)) != 0) return ZL_EINVAL;
+  const bool fused = (flags & ZL_FWD_FUSED_MERGE) != 0 && dtype == ZL_BF16;
   if (dtype != ZL_BF16 && dtype != ZL_FP32) return ZL_EUNSUPPORTED;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return ZL_EINVAL;
   Plan plan;
@@ -442,7 +466,7 @@ zl_status zl_varlen_attn_fwd(const void* q, const void* k, const void* v, const 
   if (st != ZL_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  const std::vector<Segment> segs = schedule_fwd(plan, cu_seqlens_q, cu_seqlens_k, num_seqs);
+  const std::vector<Segment> segs = schedule_fwd(plan, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads);
   static thread_local FwdArgs args;   // ~27 KB: kept off the stack
   std::memset(&args, 0, sizeof(args));
   args.o = o;
@@ -454,9 +478,16 @@ zl_status zl_varlen_attn_fwd(const void* q, const void* k, const void* v, const 
   if (need > 0) {
     char* ws = static_cast<char*>(workspace);
     args.o_part = reinterpret_cast<float*>(ws);
-    args.lse_part = reinterpret_cast<float*>(
-        ws + align256(static_cast<size_t>(plan.n_parts) * plan.part_rows * num_heads * head_dim * sizeof(float)));
+    const size_t o_bytes = align256(static_cast<size_t>(plan.n_parts) * plan.part_rows * num_heads * head_dim * sizeof(float));
+    const size_t l_bytes = align256(static_cast<size_t>(plan.n_parts) * num_heads * plan.part_rows * sizeof(float));
+    args.lse_part = reinterpret_cast<float*>(ws + o_bytes);
+    args.counters = reinterpret_cast<int32_t*>(ws + o_bytes + l_bytes);
     args.part_rows = plan.part_rows;
+    args.fused_merge = fused ? 1 : 0;
+    if (fused) {
+      st = cuda_status(cudaMemsetAsync(args.counters, 0, static_cast<size_t>(plan.n_counters) * sizeof(int32_t), s));
+      if (st != ZL_OK) return st;
+    }
   }
   CUtensorMap mq, mk, mv;
   if (dtype == ZL_BF16) {
@@ -479,9 +510,11 @@ zl_status zl_varlen_attn_fwd(const void* q, const void* k, const void* v, const 
     }
     if (st != ZL_OK) return st;
   }
-  // Combine each split sequence's partial slots into its rows of o and lse.
+  // Combine each split sequence's partial slots into its rows of o and lse
+  // (unless the forward kernel merged them in its last arriving tiles).
   const size_t esz = dtype == ZL_BF16 ? 2 : 4;
   for (const SplitSeq& sp : plan.splits) {
+    if (fused) break;
     zl::MergeArgs m;
     m.o_part = args.o_part + static_cast<size_t>(sp.rbase) * num_heads * head_dim;
     m.lse_part = args.lse_part + sp.rbase;

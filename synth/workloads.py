@@ -109,6 +109,9 @@ def config(n: int) -> Workload:
     5  training step: one 720p 81-frame video as a 2 x 2 tile grid, two 480p
        81-frame videos, 4 images of 4096 and 32 of 1024 tokens; 40 heads
     6  profiling case: one 480p 81-frame video (32,760 tokens), 24 heads
+    7  the Fig. 2 batch of the Zellige paper: three 720p 10-second videos
+       (147,600 tokens, each as a 2 x 2 tile grid) and 228 720p images
+       (3,600 tokens); 12 heads, d = 128 (Wan2.1-1.3B)
     """
     v480_81 = video_tokens(81, *RESOLUTIONS["480p"])     # 32,760
     v480_33 = video_tokens(33, *RESOLUTIONS["480p"])     # 14,040
@@ -132,6 +135,14 @@ def config(n: int) -> Workload:
     if n == 6:
         # profiling case: one long video alone, fewer heads (inputs ~200 MB)
         return Workload("video_32k_h24", [v480_81], 24, 128)
+    if n == 7:
+        # the paper's Fig. 2 batch: three 720p 10-second videos (161 frames at
+        # 16 fps) and 228 720p images, with Wan2.1-1.3B's 12 heads of 128;
+        # each video runs as a 2 x 2 tile grid beside the whole images
+        v720_161 = video_tokens(161, *RESOLUTIONS["720p"])   # 147,600
+        img720 = image_tokens(*RESOLUTIONS["720p"])          # 3,600
+        return Workload("fig2_mix", [v720_161] * 3 + [img720] * 228, 12, 128,
+                        splits={0: (2, 2), 1: (2, 2), 2: (2, 2)})
     raise ValueError(f"no workload {n}")
 
 

@@ -163,6 +163,15 @@ def test_train_step_mix_sampled():
     _sampled_check(wl, inp, o, lse, n_random=512, max_heads_long=3)
 
 
+def test_fig2_mix_sampled():
+    """The paper's Fig. 2 batch (three 147,600-token videos as 2 x 2 tiles and
+    228 images of 3,600 tokens, 12 heads) through the same engine."""
+    wl = synth.config(7)
+    inp = synth.make_inputs(wl, seed=0, device="cuda", with_grad_out=False)
+    o, lse = _run(inp, wl, wl.tiles())
+    _sampled_check(wl, inp, o, lse, n_random=256, max_heads_long=3)
+
+
 def test_sequence_isolation_bitwise():
     """§IV-D keeps sequences separate: changing one sequence's q/k/v leaves
     every other sequence's output bit-identical; outputs stay in input order."""
@@ -205,6 +214,32 @@ def test_lse_merge_standalone(hd, out_dtype):
 def test_launch_counter_and_no_errors():
     wl = synth.config(1)
     inp = synth.make_inputs(wl, seed=0, device="cuda", with_grad_out=False)
+    cu = wl.cu_seqlens()
+    tiles = synth.grid_tiles(3, 256, 256, 2, 2)
     n0 = zl.launch_count()
-    _run(inp, wl, synth.grid_tiles(3, 256, 256, 2, 2))
+    _run(inp, wl, tiles)
     assert zl.launch_count() - n0 == 2     # one attention launch + one merge
+    n0 = zl.launch_count()
+    zl.varlen_attn_fwd(inp["q"], inp["k"], inp["v"], cu, cu, tiles=tiles, fused_merge=True)
+    zl.sync_check()
+    assert zl.launch_count() - n0 == 1     # the merge happens inside the attention launch
+
+
+@pytest.mark.parametrize("n,hd", [(1, 64), (4, 128)])
+def test_fused_merge_matches_separate_merge(n, hd):
+    """The in-launch (last-arriving tile) merge gives the same result as the
+    merge kernel: the same float32 partials combined by the same identity."""
+    if n == 1:
+        wl = synth.Workload("tiny", [37, 64, 100, 256], 2, hd)
+        tiles = synth.grid_tiles(3, 256, 256, 2, 2) + synth.grid_tiles(2, 100, 100, 3, 2)
+    else:
+        wl = synth.Workload("split", [20000, 1024, 5000], 4, hd)
+        tiles = synth.grid_tiles(0, 20000, 20000, 3, 4) + synth.grid_tiles(2, 5000, 5000, 1, 3)
+    inp = synth.make_inputs(wl, seed=3, device="cuda", with_grad_out=False)
+    cu = wl.cu_seqlens()
+    o1, l1 = zl.varlen_attn_fwd(inp["q"], inp["k"], inp["v"], cu, cu, tiles=tiles)
+    o2, l2 = zl.varlen_attn_fwd(inp["q"], inp["k"], inp["v"], cu, cu, tiles=tiles, fused_merge=True)
+    zl.sync_check()
+    assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+    assert (l1 - l2).abs().max().item() <= 1e-5
+    _full_check(inp["q"], inp["k"], inp["v"], cu, cu, o2, l2, TOL_O_BF16, TOL_LSE) if n == 1 else None

@@ -338,6 +338,10 @@ def test_workload_shapes():
     totals = {1: 457, 2: 28672, 3: 118184, 4: 196608, 5: 190272}
     for n, t in totals.items():
         assert synth.config(n).total_tokens == t
+    # Fig. 2 of the paper: three 720p 10 s videos (41 x 45 x 80) and 228 720p images (45 x 80)
+    wl7 = synth.config(7)
+    assert wl7.seqlens[:3] == [41 * 45 * 80] * 3 and wl7.seqlens[3:] == [45 * 80] * 228
+    assert wl7.num_heads == 12 and len(wl7.tiles()) == 12
     assert len(synth.config(4).tiles()) == 16
     assert len(synth.config(5).tiles()) == 4
     for n in (4, 5):

@@ -1,0 +1,47 @@
+"""The single-GPU price table (the per-bucket slice of the Zellige paper's
+Hardware Profiler, arXiv 2608.01150v1 §IV-B) and its additive model."""
+import math
+
+import pytest
+
+from mixed_length_dit_gb300 import profiler
+
+
+def test_catalog_matches_paper_token_counts():
+    names = {b.name: b.tokens for b in profiler.catalog()}
+    # §I: a 15-second 1080p video is 497,760 tokens; Fig. 1: a 256p image is 256
+    assert names["vid_1080p_15s"] == 497760
+    assert names["img_256p"] == 256
+    # Fig. 2: a 720p 10-second video is 41 x 45 x 80 tokens, a 720p image 45 x 80
+    assert names["vid_720p_10s"] == 41 * 45 * 80
+    assert names["img_720p"] == 45 * 80
+    toks = [b.tokens for b in profiler.catalog()]
+    assert toks == sorted(toks)
+
+
+def test_additive_prediction():
+    bks = [profiler.Bucket("a", 1000, "image"), profiler.Bucket("b", 4000, "video")]
+    prices = {"a": 1.0, "b": 10.0}
+    assert profiler.predict_ms([1000, 1000, 4000], prices, bks) == pytest.approx(12.0)
+    # a length between buckets takes the nearest one, scaled quadratically
+    assert profiler.predict_ms([2000], prices, bks) == pytest.approx(1.0 * 4)
+    assert profiler.predict_ms([0, 3000], prices, bks) == pytest.approx(10.0 * (3000 / 4000) ** 2)
+    with pytest.raises(ValueError):
+        profiler.predict_ms([10], {}, bks)
+
+
+@pytest.mark.gpu
+def test_prices_predict_a_mixed_batch():
+    """Prices measured per bucket predict the time of a coalesced mixed batch
+    of those buckets (the additive model the paper evaluates in §V-B)."""
+    bks = [b for b in profiler.catalog() if b.name in ("img_480p", "img_1080p", "vid_480p_5s", "vid_720p_5s")]
+    prices = profiler.measure_prices(bks, num_heads=12, fill_tokens=200_000, reps=3)
+    for b in bks:
+        assert prices[b.name] > 0
+    # quadratic work: a longer bucket costs more per sequence
+    by = sorted(bks, key=lambda b: b.tokens)
+    assert all(prices[x.name] < prices[y.name] for x, y in zip(by, by[1:]))
+    mix = [b.tokens for b in bks for _ in range(6)]
+    measured = profiler.time_batch(mix, num_heads=12)
+    predicted = profiler.predict_ms(mix, prices, bks)
+    assert abs(predicted - measured) / measured < 0.25, (predicted, measured)

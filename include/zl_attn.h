@@ -62,18 +62,27 @@ typedef enum {
 } zl_dtype;
 
 /*
- * One (query-chunk x KV-chunk) tile of a split sequence.  Zellige §IV-D runs
- * shards of split sequences alongside whole ones; §II-B and Table II describe
- * how a split sequence's attention is computed from K/V blocks and
- * accumulated exactly.  Offsets are relative to the sequence's own query and
- * key ranges.
+ * One (query-chunk x head-range x KV-chunk) tile of a split sequence.
+ * Zellige §IV-A gives every sequence a parallelism configuration (q, h, k):
+ * split factors along the query axis (all-gather), the head axis (Ulysses) and
+ * the key/value axis (ring), composable, (1, 1, 1) meaning whole; §IV-D runs
+ * the shards of split sequences alongside whole ones, and §II-B / Table II
+ * describe how a key-split sequence's attention is accumulated exactly from
+ * its K/V blocks.  A tile is one shard of such a configuration.  Offsets are
+ * relative to the sequence's own query and key ranges; heads are absolute.
  *
- * The tiles of a sequence must form a full grid: n_q_chunks x n_kv_chunks
- * tiles, one per (q_chunk, kv_chunk), whose query ranges partition the
- * sequence's queries and whose key ranges partition its keys (every tile with
- * the same q_chunk has the same query range, every tile with the same kv_chunk
- * the same key range, chunk ranges contiguous and in chunk order, no empty
- * chunk).  A sequence listed in the tile table is not also run whole.
+ * The tiles of a sequence must form a full grid: n_h_chunks x n_q_chunks x
+ * n_kv_chunks tiles, one per (h_chunk, q_chunk, kv_chunk), whose head ranges
+ * partition [0, H), whose query ranges partition the sequence's queries and
+ * whose key ranges partition its keys (every tile with the same h_chunk has
+ * the same head range, every tile with the same q_chunk the same query range,
+ * every tile with the same kv_chunk the same key range; chunk ranges
+ * contiguous, in chunk order, none empty).  A sequence listed in the tile
+ * table is not also run whole.  A sequence with n_kv_chunks = 1 (a (q, h, 1)
+ * configuration) needs no merge: its tiles write o and lse directly.
+ *
+ * h_len = 0 selects all H heads (h_start and h_chunk must then be 0), so a
+ * zero-initialised head range means "not split by heads".
  */
 typedef struct {
   int32_t seq;          /* index into cu_seqlens_q / cu_seqlens_k             */
@@ -84,6 +93,9 @@ typedef struct {
   int32_t q_chunk;      /* 0 .. n_q_chunks-1                                  */
   int32_t kv_chunk;     /* 0 .. n_kv_chunks-1: the partial slot it writes     */
   int32_t n_kv_chunks;  /* same for every tile of the sequence, 1 .. 64       */
+  int32_t h_start;      /* first head of the tile's head range                */
+  int32_t h_len;        /* heads in the range, 0 = all H heads                */
+  int32_t h_chunk;      /* 0 .. n_h_chunks-1                                  */
 } zl_tile_t;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -94,9 +106,10 @@ int32_t zl_version(void);
 
 /*
  * Workspace needed by zl_varlen_attn_fwd for this batch, in bytes (0 when no
- * sequence is split).  It holds the float32 shard partials: for the split
- * sequences (in sequence order, R = sum of their query lengths, P = largest
- * n_kv_chunks) an O partial [P][R][H][d] and an LSE partial [P][H][R].
+ * sequence is split along its keys).  It holds the float32 shard partials:
+ * for the sequences with n_kv_chunks > 1 (in sequence order, R = sum of their
+ * query lengths, P = largest n_kv_chunks) an O partial [P][R][H][d] and an
+ * LSE partial [P][H][R], then the fused-merge arrival counters.
  * Same argument rules as zl_varlen_attn_fwd.  Writes the size to *bytes.
  */
 zl_status zl_varlen_attn_fwd_workspace_size(
@@ -117,11 +130,13 @@ zl_status zl_varlen_attn_fwd_workspace_size(
  * workspace                    device, >= zl_varlen_attn_fwd_workspace_size
  *
  * Whole sequences and every tile run in one persistent launch whose work
- * items (sequence-or-tile x head x 128-query block) are ordered longest
- * first, ties in input order.  Tiles write float32 partials into the
- * workspace, and a merge launch per split sequence (zl_lse_merge's kernel)
- * then combines each query row's partials into o and lse exactly.  A sequence with queries but no
- * keys is rejected (ZL_EINVAL); zero-length sequences are skipped.
+ * items (sequence-or-tile x head of its range x 128-query block) are ordered
+ * longest first, ties in input order.  Tiles of key-split sequences write
+ * float32 partials into the workspace, and a merge launch per such sequence
+ * (zl_lse_merge's kernel) then combines each query row's partials into o and
+ * lse exactly; tiles of sequences split only by queries and heads write o and
+ * lse directly.  A sequence with queries but no keys is rejected (ZL_EINVAL);
+ * zero-length sequences are skipped.
  */
 zl_status zl_varlen_attn_fwd(
     const void* q, const void* k, const void* v,

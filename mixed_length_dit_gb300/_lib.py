@@ -38,7 +38,8 @@ ZL_FWD_FUSED_MERGE = 1
 class Tile(ctypes.Structure):
     """zl_tile_t"""
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("seq", "q_start", "q_len", "k_start", "k_len", "q_chunk", "kv_chunk", "n_kv_chunks")]
+                ("seq", "q_start", "q_len", "k_start", "k_len", "q_chunk", "kv_chunk", "n_kv_chunks",
+                 "h_start", "h_len", "h_chunk")]
 
 
 class ProfileEntry(ctypes.Structure):
@@ -119,12 +120,15 @@ def int32_array(values):
 
 def tile_array(tiles):
     """Host zl_tile_t array from tuples (seq, q_start, q_len, k_start, k_len,
-    q_chunk, kv_chunk, n_kv_chunks)."""
+    q_chunk, kv_chunk, n_kv_chunks[, h_start, h_len, h_chunk]); a tuple of
+    eight leaves the head range zero, i.e. all heads."""
     if not tiles:
         return None, 0
     arr = (Tile * len(tiles))()
+    names = [f[0] for f in Tile._fields_]
     for i, t in enumerate(tiles):
-        for name, val in zip(("seq", "q_start", "q_len", "k_start", "k_len", "q_chunk", "kv_chunk",
-                              "n_kv_chunks"), t):
+        if len(t) not in (8, 11):
+            raise ValueError("a tile has 8 or 11 fields")
+        for name, val in zip(names, t):
             setattr(arr[i], name, int(val))
     return arr, len(tiles)

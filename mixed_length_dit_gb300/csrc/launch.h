@@ -16,18 +16,20 @@ constexpr int kBlockN = 128;
 constexpr int kMaxSegs = 640;
 
 // One segment of forward work: a whole sequence or one shard tile.  Its work
-// items are (head, 128-row query block) pairs, numbered from item0 with the
-// query block fastest.
+// items are (head of [h0, h0 + nh), 128-row query block) pairs, numbered from
+// item0 with the query block fastest.
 struct FwdSeg {
   int32_t q_row0;    // packed row of the segment's first query
   int32_t k_row0;    // packed row of the segment's first key
   int32_t q_len;     // >= 1
   int32_t k_len;     // >= 1
-  int32_t out_row0;  // whole: = q_row0 (row in o/lse); tile: row in the partial slot
-  int32_t slot;      // -1: whole sequence, else the partial slot (kv chunk)
+  int32_t out_row0;  // slot < 0: row in o/lse; else row in the partial slot
+  int32_t slot;      // -1: writes o/lse directly, else the partial slot (kv chunk)
   int32_t item0;     // first work item of the segment
   int32_t counter0;  // tile: first arrival counter of its query chunk (+ qb * H + h)
   int32_t n_kv;      // tile: kv chunks of its sequence (partials to merge)
+  int32_t h0;        // first head
+  int32_t nh;        // heads, >= 1
 };
 
 struct FwdArgs {
@@ -46,6 +48,7 @@ struct FwdArgs {
   int32_t n_segs;
   FwdSeg segs[kMaxSegs];
 };
+static_assert(sizeof(FwdArgs) <= 32764, "forward arguments exceed the kernel parameter space");
 
 struct MergeArgs {
   const float* o_part;

@@ -1,5 +1,6 @@
 // Work-item decoding shared by the forward kernels: the host scheduler
-// numbers items segment by segment (head-major, 128-row query block fastest).
+// numbers items segment by segment (head-major over the segment's head range,
+// 128-row query block fastest).
 #pragma once
 #include "launch.h"
 
@@ -20,7 +21,7 @@ __device__ __forceinline__ FwdWork decode_fwd(const FwdArgs& a, int it) {
   const FwdSeg& s = a.segs[lo];
   const int nqb = (s.q_len + kBlockM - 1) / kBlockM;
   const int local = it - s.item0;
-  return {lo, local / nqb, local % nqb};
+  return {lo, s.h0 + local / nqb, local % nqb};
 }
 
 }  // namespace zl

@@ -175,15 +175,17 @@ bool make_map_acc(CUtensorMap* map, const float* base, int64_t rows, int nh, int
 struct SplitSeq {
   int seq = 0;
   int n_kv = 0;
-  int64_t rbase = 0;   // first row of this sequence in every partial slot
-  int64_t len = 0;     // query length
+  bool merged = false;   // n_kv > 1: tiles write partials, a merge combines them
+  int64_t rbase = 0;     // merged: first row of this sequence in every partial slot
+  int64_t len = 0;       // query length
+  std::vector<int64_t> counter0;   // merged: first arrival counter of each query chunk
 };
 
 struct Plan {
   int64_t tq = 0, tk = 0;
   std::vector<int> split_index;     // per sequence: -1, or index into splits
   std::vector<SplitSeq> splits;
-  std::vector<zl_tile_t> tiles;     // sorted by (seq, q_chunk, kv_chunk)
+  std::vector<zl_tile_t> tiles;     // sorted by (seq, h_chunk, q_chunk, kv_chunk), h_len resolved
   int64_t part_rows = 0;            // R
   int n_parts = 0;                  // P
   int64_t n_counters = 0;           // arrival counters: (query chunk, 128-row block) x head
@@ -220,7 +222,7 @@ zl_status make_plan(const int32_t* cu_q, const int32_t* cu_k, int32_t b, int32_t
   if (n_tiles == 0) return ZL_OK;
   if (!tiles) return ZL_EINVAL;
   plan->tiles.assign(tiles, tiles + n_tiles);
-  for (const zl_tile_t& t : plan->tiles) {
+  for (zl_tile_t& t : plan->tiles) {
     if (t.seq < 0 || t.seq >= b) return ZL_EINVAL;
     const int64_t lq = cu_q[t.seq + 1] - cu_q[t.seq];
     const int64_t lk = cu_k[t.seq + 1] - cu_k[t.seq];
@@ -229,24 +231,37 @@ zl_status make_plan(const int32_t* cu_q, const int32_t* cu_k, int32_t b, int32_t
       return ZL_EINVAL;
     if (t.q_len < 1 || t.k_len < 1 || t.q_start < 0 || t.k_start < 0) return ZL_EINVAL;
     if (int64_t(t.q_start) + t.q_len > lq || int64_t(t.k_start) + t.k_len > lk) return ZL_EINVAL;
+    if (t.h_len == 0) {
+      if (t.h_start != 0 || t.h_chunk != 0) return ZL_EINVAL;
+      t.h_len = nh;
+    }
+    if (t.h_start < 0 || t.h_len < 1 || int64_t(t.h_start) + t.h_len > nh) return ZL_EINVAL;
+    if (t.h_chunk < 0 || t.h_chunk >= nh) return ZL_EINVAL;
   }
   std::stable_sort(plan->tiles.begin(), plan->tiles.end(), [](const zl_tile_t& a, const zl_tile_t& c) {
     if (a.seq != c.seq) return a.seq < c.seq;
+    if (a.h_chunk != c.h_chunk) return a.h_chunk < c.h_chunk;
     if (a.q_chunk != c.q_chunk) return a.q_chunk < c.q_chunk;
     return a.kv_chunk < c.kv_chunk;
   });
-  // Each split sequence: a full n_q x n_kv grid of tiles partitioning its
-  // query range and its key range into contiguous chunks in chunk order.
+  // Each split sequence: a full n_h x n_q x n_kv grid.  Head chunk 0's tiles
+  // are an n_q x n_kv grid partitioning the query range and the key range
+  // into contiguous chunks in chunk order; every further head chunk repeats
+  // that grid exactly over the next contiguous head range.
   size_t i = 0;
   int64_t rbase = 0;
   while (i < plan->tiles.size()) {
     const int seq = plan->tiles[i].seq;
     size_t j = i;
     while (j < plan->tiles.size() && plan->tiles[j].seq == seq) ++j;
+    size_t g = i;   // end of head chunk 0
+    while (g < j && plan->tiles[g].h_chunk == plan->tiles[i].h_chunk) ++g;
+    const size_t per_h = g - i;
+    if ((j - i) % per_h != 0) return ZL_EINVAL;
+    const int n_h = static_cast<int>((j - i) / per_h);
     const int n_kv = plan->tiles[i].n_kv_chunks;
-    const size_t cnt = j - i;
-    if (cnt % static_cast<size_t>(n_kv) != 0) return ZL_EINVAL;
-    const int n_q = static_cast<int>(cnt / static_cast<size_t>(n_kv));
+    if (per_h % static_cast<size_t>(n_kv) != 0) return ZL_EINVAL;
+    const int n_q = static_cast<int>(per_h / static_cast<size_t>(n_kv));
     const int64_t lq = cu_q[seq + 1] - cu_q[seq];
     const int64_t lk = cu_k[seq + 1] - cu_k[seq];
     int64_t q_expect = 0;
@@ -267,30 +282,48 @@ zl_status make_plan(const int32_t* cu_q, const int32_t* cu_k, int32_t b, int32_t
       q_expect += first.q_len;
     }
     if (q_expect != lq) return ZL_EINVAL;
-    for (int qc = 0; qc < n_q; ++qc) {
-      const zl_tile_t& first = plan->tiles[i + static_cast<size_t>(qc) * n_kv];
-      plan->n_counters += (first.q_len + kBlockM - 1) / kBlockM;   // times H below
+    int64_t h_expect = 0;
+    for (int hc = 0; hc < n_h; ++hc) {
+      const zl_tile_t& h_first = plan->tiles[i + static_cast<size_t>(hc) * per_h];
+      if (h_first.h_start != h_expect) return ZL_EINVAL;
+      for (size_t x = 0; x < per_h; ++x) {
+        const zl_tile_t& t = plan->tiles[i + static_cast<size_t>(hc) * per_h + x];
+        const zl_tile_t& ref = plan->tiles[i + x];   // same position in head chunk 0
+        if (t.h_chunk != hc || t.h_start != h_first.h_start || t.h_len != h_first.h_len) return ZL_EINVAL;
+        if (t.q_chunk != ref.q_chunk || t.kv_chunk != ref.kv_chunk || t.n_kv_chunks != n_kv ||
+            t.q_start != ref.q_start || t.q_len != ref.q_len || t.k_start != ref.k_start || t.k_len != ref.k_len)
+          return ZL_EINVAL;
+      }
+      h_expect += h_first.h_len;
     }
+    if (h_expect != nh) return ZL_EINVAL;
     SplitSeq sp;
     sp.seq = seq;
     sp.n_kv = n_kv;
-    sp.rbase = rbase;
+    sp.merged = n_kv > 1;
     sp.len = lq;
+    if (sp.merged) {
+      sp.rbase = rbase;
+      rbase += lq;
+      plan->n_parts = std::max(plan->n_parts, n_kv);
+      for (int qc = 0; qc < n_q; ++qc) {
+        const zl_tile_t& first = plan->tiles[i + static_cast<size_t>(qc) * n_kv];
+        sp.counter0.push_back(plan->n_counters);
+        plan->n_counters += int64_t((first.q_len + kBlockM - 1) / kBlockM) * nh;
+      }
+    }
     plan->split_index[static_cast<size_t>(seq)] = static_cast<int>(plan->splits.size());
-    plan->splits.push_back(sp);
-    rbase += lq;
-    plan->n_parts = std::max(plan->n_parts, n_kv);
+    plan->splits.push_back(std::move(sp));
     i = j;
   }
   plan->part_rows = rbase;
-  plan->n_counters *= nh;
   return ZL_OK;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t fwd_workspace_bytes(const Plan& p, int nh, int hd) {
-  if (p.splits.empty()) return 0;
+  if (p.part_rows == 0) return 0;
   const size_t o_bytes = static_cast<size_t>(p.n_parts) * p.part_rows * nh * hd * sizeof(float);
   const size_t l_bytes = static_cast<size_t>(p.n_parts) * nh * p.part_rows * sizeof(float);
   const size_t c_bytes = static_cast<size_t>(p.n_counters) * sizeof(int32_t);
@@ -307,7 +340,6 @@ struct Segment {
 // Whole sequences and tiles as segments, stably ordered by decreasing cost.
 std::vector<Segment> schedule_fwd(const Plan& p, const int32_t* cu_q, const int32_t* cu_k, int32_t b, int nh) {
   std::vector<Segment> segs;
-  int64_t counter_base = 0, counter_next = 0;   // arrival counters of the query chunks, in tile order
   segs.reserve(static_cast<size_t>(b) + p.tiles.size());
   size_t ti = 0;
   int order = 0;
@@ -318,7 +350,7 @@ std::vector<Segment> schedule_fwd(const Plan& p, const int32_t* cu_q, const int3
     if (si < 0) {
       if (lq == 0) continue;
       Segment g;
-      g.seg = FwdSeg{cu_q[s], cu_k[s], lq, lk, cu_q[s], -1, 0, 0, 0};
+      g.seg = FwdSeg{cu_q[s], cu_k[s], lq, lk, cu_q[s], -1, 0, 0, 0, 0, nh};
       g.cost = lk;
       g.order = order++;
       segs.push_back(g);
@@ -327,14 +359,16 @@ std::vector<Segment> schedule_fwd(const Plan& p, const int32_t* cu_q, const int3
       while (ti < p.tiles.size() && p.tiles[ti].seq < s) ++ti;
       for (; ti < p.tiles.size() && p.tiles[ti].seq == s; ++ti) {
         const zl_tile_t& t = p.tiles[ti];
-        if (t.kv_chunk == 0) {               // first tile of a new query chunk
-          counter_base += counter_next;
-          counter_next = static_cast<int64_t>((t.q_len + kBlockM - 1) / kBlockM) * nh;
-        }
         Segment g;
-        g.seg = FwdSeg{cu_q[s] + t.q_start, cu_k[s] + t.k_start, t.q_len, t.k_len,
-                       static_cast<int32_t>(sp.rbase + t.q_start), t.kv_chunk, 0,
-                       static_cast<int32_t>(counter_base), sp.n_kv};
+        if (sp.merged) {
+          g.seg = FwdSeg{cu_q[s] + t.q_start, cu_k[s] + t.k_start, t.q_len, t.k_len,
+                         static_cast<int32_t>(sp.rbase + t.q_start), t.kv_chunk, 0,
+                         static_cast<int32_t>(sp.counter0[static_cast<size_t>(t.q_chunk)]), sp.n_kv,
+                         t.h_start, t.h_len};
+        } else {   // one kv chunk: the tile's rows are final
+          g.seg = FwdSeg{cu_q[s] + t.q_start, cu_k[s] + t.k_start, t.q_len, t.k_len,
+                         cu_q[s] + t.q_start, -1, 0, 0, 0, t.h_start, t.h_len};
+        }
         g.cost = t.k_len;
         g.order = order++;
         segs.push_back(g);
@@ -347,14 +381,14 @@ std::vector<Segment> schedule_fwd(const Plan& p, const int32_t* cu_q, const int3
 }
 
 // Fills args.segs with segments [first, last) and numbers their items.
-void fill_args(FwdArgs* args, const std::vector<Segment>& segs, size_t first, size_t last, int nh) {
+void fill_args(FwdArgs* args, const std::vector<Segment>& segs, size_t first, size_t last) {
   int64_t items = 0;
   args->n_segs = static_cast<int32_t>(last - first);
   for (size_t i = first; i < last; ++i) {
     FwdSeg s = segs[i].seg;
     s.item0 = static_cast<int32_t>(items);
     args->segs[i - first] = s;
-    items += int64_t(nh) * ((s.q_len + kBlockM - 1) / kBlockM);
+    items += int64_t(s.nh) * ((s.q_len + kBlockM - 1) / kBlockM);
   }
   args->n_items = static_cast<int32_t>(items);
 }
@@ -388,7 +422,7 @@ const char* zl_status_string(int32_t status) {
   }
 }
 
-int32_t zl_version(void) { return (1 << 16) | 0; }
+int32_t zl_version(void) { return (2 << 16) | 0; }
 
 int64_t zl_launch_count(void) { return g_launches.load(); }
 
@@ -497,7 +531,7 @@ zl_status zl_varlen_attn_fwd_ex(const void* q, const void* k, const void* v, con
   }
   for (size_t first = 0; first < segs.size(); first += kMaxSegs) {
     const size_t last = std::min(segs.size(), first + kMaxSegs);
-    fill_args(&args, segs, first, last, num_heads);
+    fill_args(&args, segs, first, last);
     if (args.n_items == 0) continue;
     if (dtype == ZL_BF16) {
       const int grid = std::min(args.n_items, 2 * sms);
@@ -515,6 +549,7 @@ zl_status zl_varlen_attn_fwd_ex(const void* q, const void* k, const void* v, con
   const size_t esz = dtype == ZL_BF16 ? 2 : 4;
   for (const SplitSeq& sp : plan.splits) {
     if (fused) break;
+    if (!sp.merged) continue;
     zl::MergeArgs m;
     m.o_part = args.o_part + static_cast<size_t>(sp.rbase) * num_heads * head_dim;
     m.lse_part = args.lse_part + sp.rbase;

@@ -2,6 +2,6 @@
 from .attn_f64 import (  # noqa: F401
     ROW_BLOCK, attention_f64, attention_rows, attention_bwd_f64, default_scale,
     dkdv_rows, dq_rows, grad_k, grad_q, grad_scores, grad_v, lse_merge, probabilities,
-    row_logsumexp, scores, tile_partial,
+    row_logsumexp, scores, tile_heads, tile_partial, tiled_attn_fwd,
     varlen_attn_bwd, varlen_attn_fwd,
 )

@@ -18,6 +18,10 @@ DiT Training", arXiv 2608.01150v1):
   exact attention.  The pages print no merge formula; the exact combination of
   (partial O, log-sum-exp) pairs is the plain identity of the softmax:
   lse = log sum_j exp(lse_j),  O = sum_j exp(lse_j - lse) O_j.
+* §IV-A / Table II: a split sequence takes a configuration (q, h, k) that cuts
+  its queries (all-gather), its heads (Ulysses) and its keys (ring).  Heads are
+  independent, and a query chunk with all of its keys is final; only the key
+  axis needs the merge above.
 * Backward: the analytic gradient of softmax(Q K^T * scale) V.  The pages do not
   print it (they train with exact backward, §V-A); it is plain calculus.
 
@@ -37,8 +41,10 @@ Layouts (all float64 numpy arrays):
   cu_q, cu_k   [B+1] int      prefix sums of per-sequence lengths, cu[0] = 0
   o            [Tq, H, d]
   lse          [H, Tq]        head-major
-  tile         (seq, q_start, q_len, k_start, k_len)  offsets relative to the
-               sequence's own query / key ranges
+  tile         (seq, q_start, q_len, k_start, k_len, q_chunk, kv_chunk,
+               n_kv_chunks[, h_start, h_len, h_chunk])  offsets relative to
+               the sequence's own query / key ranges; heads absolute, a
+               missing or zero-length head range meaning all heads
 """
 from __future__ import annotations
 
@@ -141,24 +147,64 @@ def attention_rows(q, k, v, cu_q, cu_k, seq, head, rows, scale=None):
 # Table II; §IV-D runs such shards alongside whole sequences).
 # --------------------------------------------------------------------------
 
+def tile_heads(tile, num_heads: int):
+    """The heads a tile covers: [h_start, h_start + h_len), or all of them
+    when the tile has no head range or h_len = 0."""
+    if len(tile) > 9 and int(tile[9]) > 0:
+        return list(range(int(tile[8]), int(tile[8]) + int(tile[9])))
+    return list(range(num_heads))
+
+
 def tile_partial(q, k, v, cu_q, cu_k, tile, scale=None):
-    """Attention of one (query-chunk x KV-chunk) tile of a split sequence,
-    restricted to that tile's keys.  Returns the partial o [q_len,H,d] and its
-    own log-sum-exp [H,q_len]."""
+    """Attention of one (query-chunk x head-range x KV-chunk) tile of a split
+    sequence, restricted to that tile's keys and heads.  Returns the partial
+    o [q_len, h, d] and its own log-sum-exp [h, q_len] for the tile's h heads
+    (tile_heads order)."""
     seq, q_start, q_len, k_start, k_len = (int(x) for x in tile[:5])
     d = q.shape[2]
     if scale is None:
         scale = default_scale(d)
     qa = int(cu_q[seq]) + q_start
     ka = int(cu_k[seq]) + k_start
-    nh = q.shape[1]
-    o = np.zeros((q_len, nh, v.shape[2]), dtype=np.float64)
-    lse = np.full((nh, q_len), -np.inf, dtype=np.float64)
-    for h in range(nh):
+    heads = tile_heads(tile, q.shape[1])
+    o = np.zeros((q_len, len(heads), v.shape[2]), dtype=np.float64)
+    lse = np.full((len(heads), q_len), -np.inf, dtype=np.float64)
+    for i, h in enumerate(heads):
         o_h, l_h = attention_f64(q[qa:qa + q_len, h], k[ka:ka + k_len, h],
                                  v[ka:ka + k_len, h], scale)
-        o[:, h] = o_h
-        lse[h] = l_h
+        o[:, i] = o_h
+        lse[i] = l_h
+    return o, lse
+
+
+def tiled_attn_fwd(q, k, v, cu_q, cu_k, tiles, scale=None):
+    """The packed forward with some sequences split by a tile table: whole
+    sequences as varlen_attn_fwd; for a split sequence every (head range,
+    query range) takes the partials of its KV chunks and combines them with
+    lse_merge (one chunk passes through).  Returns o [Tq,H,d], lse [H,Tq]."""
+    tq, nh, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    split = sorted({int(t[0]) for t in tiles})
+    whole = [s for s in range(len(cu_q) - 1) if s not in split]
+    o = np.zeros((tq, nh, v.shape[2]), dtype=np.float64)
+    lse = np.full((nh, tq), -np.inf, dtype=np.float64)
+    for s in whole:
+        qa, qb = int(cu_q[s]), int(cu_q[s + 1])
+        ka, kb = int(cu_k[s]), int(cu_k[s + 1])
+        for h in range(nh):
+            o[qa:qb, h], lse[h, qa:qb] = attention_f64(q[qa:qb, h], k[ka:kb, h], v[ka:kb, h], scale)
+    groups = {}
+    for t in tiles:
+        key = (int(t[0]), int(t[1]), int(t[2]), tuple(tile_heads(t, nh)))
+        groups.setdefault(key, []).append(t)
+    for (s, q_start, q_len, heads), ts in groups.items():
+        parts = [tile_partial(q, k, v, cu_q, cu_k, t, scale) for t in ts]
+        om, lm = lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+        r0 = int(cu_q[s]) + q_start
+        for i, h in enumerate(heads):
+            o[r0:r0 + q_len, h] = om[:, i]
+            lse[h, r0:r0 + q_len] = lm[i]
     return o, lse
 
 

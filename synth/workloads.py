@@ -49,7 +49,7 @@ class Workload:
     seqlens: list          # packed order == listed order
     num_heads: int
     head_dim: int
-    splits: dict = field(default_factory=dict)  # seq index -> (n_q_chunks, n_kv_chunks)
+    splits: dict = field(default_factory=dict)  # seq index -> (n_q, n_kv) or (n_q, n_kv, n_h) chunks
     dtype: str = "bf16"
 
     @property
@@ -65,8 +65,10 @@ class Workload:
     def tiles(self):
         """Tile table of the split sequences (see chunk_bounds)."""
         out = []
-        for s, (nq, nk) in sorted(self.splits.items()):
-            out.extend(grid_tiles(s, self.seqlens[s], self.seqlens[s], nq, nk))
+        for s, sp in sorted(self.splits.items()):
+            nq, nk = sp[0], sp[1]
+            nh = sp[2] if len(sp) > 2 else 1
+            out.extend(grid_tiles(s, self.seqlens[s], self.seqlens[s], nq, nk, nh, self.num_heads))
         return out
 
     def pair_count(self) -> int:
@@ -87,18 +89,31 @@ def chunk_bounds(length: int, n: int):
     return out
 
 
-def grid_tiles(seq: int, q_len: int, k_len: int, n_q: int, n_kv: int):
-    """The full (query-chunk x KV-chunk) grid of one split sequence as tuples
-    (seq, q_start, q_len, k_start, k_len, q_chunk, kv_chunk, n_kv_chunks)."""
+def grid_tiles(seq: int, q_len: int, k_len: int, n_q: int, n_kv: int, n_h: int = 1, num_heads: int = 0):
+    """The full (head-chunk x query-chunk x KV-chunk) grid of one split
+    sequence, the (q, h, k) parallelism configuration of the Zellige paper
+    (§IV-A), as tuples (seq, q_start, q_len, k_start, k_len, q_chunk,
+    kv_chunk, n_kv_chunks, h_start, h_len, h_chunk).  With n_h = 1 the head
+    range is left as (0, 0, 0), meaning all heads; with n_h > 1 the num_heads
+    heads are cut into chunk_bounds(num_heads, n_h)."""
     qb = chunk_bounds(q_len, n_q)
     kb = chunk_bounds(k_len, n_kv)
-    return [(seq, qa, ql, ka, kl, i, j, n_kv)
+    if n_h == 1:
+        hb = [(0, 0)]
+    else:
+        if num_heads < n_h:
+            raise ValueError("head split needs num_heads >= n_h")
+        hb = chunk_bounds(num_heads, n_h)
+        if any(hl == 0 for _, hl in hb):
+            raise ValueError(f"{num_heads} heads do not make {n_h} non-empty chunks")
+    return [(seq, qa, ql, ka, kl, i, j, n_kv, ha, hl, c)
+            for c, (ha, hl) in enumerate(hb)
             for i, (qa, ql) in enumerate(qb)
             for j, (ka, kl) in enumerate(kb)]
 
 
 def config(n: int) -> Workload:
-    """The five batches used for parity and measurement (1-based numbering).
+    """The batches used for parity and measurement (1-based numbering).
 
     1  tiny correctness batch: lengths 37, 64, 100, 256; 2 heads, d = 64
     2  image-only mix: 16 x 256, 8 x 1024, 4 x 4096 tokens; 24 heads, d = 128
@@ -112,6 +127,12 @@ def config(n: int) -> Workload:
     7  the Fig. 2 batch of the Zellige paper: three 720p 10-second videos
        (147,600 tokens, each as a 2 x 2 tile grid) and 228 720p images
        (3,600 tokens); 12 heads, d = 128 (Wan2.1-1.3B)
+    8  (q, h, k) configurations (§IV-A): one 720p 81-frame video as (1, 4, 1)
+       (Ulysses degree 4: 10 heads per shard), a 480p 81-frame video as
+       (2, 2, 2), another as (2, 5, 1), and 24 images of 1024 tokens whole;
+       40 heads, d = 128
+
+    `splits` maps a sequence to (n_q, n_kv) or (n_q, n_kv, n_h) chunk counts.
     """
     v480_81 = video_tokens(81, *RESOLUTIONS["480p"])     # 32,760
     v480_33 = video_tokens(33, *RESOLUTIONS["480p"])     # 14,040
@@ -143,6 +164,9 @@ def config(n: int) -> Workload:
         img720 = image_tokens(*RESOLUTIONS["720p"])          # 3,600
         return Workload("fig2_mix", [v720_161] * 3 + [img720] * 228, 12, 128,
                         splits={0: (2, 2), 1: (2, 2), 2: (2, 2)})
+    if n == 8:
+        return Workload("qhk_mix", [v720_81, v480_81, v480_81] + [img512] * 24, 40, 128,
+                        splits={0: (1, 1, 4), 1: (2, 2, 2), 2: (2, 1, 5)})
     raise ValueError(f"no workload {n}")
 
 

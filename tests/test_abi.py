@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strings(lib):
-    assert lib.zl_version() >> 16 == 1
+    assert lib.zl_version() >> 16 == 2
     for code in range(0, -8, -1):
         assert _lib.status_string(code) not in ("", "unknown status")
     assert _lib.status_string(-99) == "unknown status"
@@ -105,6 +105,54 @@ def test_tile_table_validation(lib):
     assert ws_size([(1, 0, 10, 0, 10, 0, 0, 1)])[0] == _lib.ZL_OK
     assert _fwd(lib, cu, cu, tiles=good, ws=0) == _lib.ZL_EWORKSPACE
     assert _fwd(lib, cu, cu, tiles=good, ws=256, ws_bytes=16) == _lib.ZL_EWORKSPACE
+
+
+def _ws(lib, cu, tiles, nh):
+    cq, nq = _lib.int32_array(cu)
+    ta, nt = _lib.tile_array(tiles)
+    out = ctypes.c_size_t(0)
+    st = lib.zl_varlen_attn_fwd_workspace_size(cq, cq, nq - 1, nh, 64, ta, nt, ctypes.byref(out))
+    return st, out.value
+
+
+def _edit(tiles, i, field, value):
+    out = list(tiles)
+    t = list(out[i])
+    t[field] = value
+    out[i] = tuple(t)
+    return out
+
+
+def test_head_sharded_tile_validation(lib):
+    """(q, h, k) configurations (Zellige §IV-A): head ranges must partition
+    [0, H) and every head chunk must repeat the same query x key grid."""
+    L, H = 300, 4
+    cu = [0, L, L + 10]
+    good = synth.grid_tiles(0, L, L, 2, 3, 2, H)             # 2 head chunks x 2 x 3
+    assert len(good) == 12
+    st, n_heads_split = _ws(lib, cu, good, H)
+    assert st == _lib.ZL_OK
+    assert n_heads_split == _ws(lib, cu, synth.grid_tiles(0, L, L, 2, 3), H)[1]   # same partials
+    assert _ws(lib, cu, list(reversed(good)), H)[0] == _lib.ZL_OK
+    assert _ws(lib, cu, good[:6], H)[0] == _lib.ZL_EINVAL            # head chunk 1 missing
+    assert _ws(lib, cu, good[:-1], H)[0] == _lib.ZL_EINVAL           # one tile missing
+    assert _ws(lib, cu, synth.grid_tiles(0, L, L, 2, 3, 2, H + 2), H)[0] == _lib.ZL_EINVAL  # beyond H
+    assert _ws(lib, cu, synth.grid_tiles(0, L, L, 2, 3, 2, H - 1), H)[0] == _lib.ZL_EINVAL  # heads left out
+    gap = [t[:8] + (t[8] + (1 if t[10] == 1 else 0), t[9] - (1 if t[10] == 1 else 0), t[10]) for t in good]
+    assert _ws(lib, cu, gap, H)[0] == _lib.ZL_EINVAL                 # heads 2 uncovered
+    assert _ws(lib, cu, _edit(good, 7, 9, 1), H)[0] == _lib.ZL_EINVAL   # ranges differ in a chunk
+    assert _ws(lib, cu, _edit(good, 7, 1, 5), H)[0] == _lib.ZL_EINVAL   # grids differ across chunks
+    whole = synth.grid_tiles(0, L, L, 2, 3)
+    assert _ws(lib, cu, _edit(whole, 0, 8, 1), H)[0] == _lib.ZL_EINVAL  # h_len 0 needs h_start 0
+    assert _ws(lib, cu, _edit(whole, 0, 10, 1), H)[0] == _lib.ZL_EINVAL  # ... and h_chunk 0
+    assert _ws(lib, cu, _edit(whole, 0, 9, -1), H)[0] == _lib.ZL_EINVAL
+    # key axis not split: no partials, so no workspace
+    assert _ws(lib, cu, synth.grid_tiles(0, L, L, 1, 1, 4, H), H) == (_lib.ZL_OK, 0)
+    assert _ws(lib, cu, synth.grid_tiles(0, L, L, 3, 1, 2, H), H) == (_lib.ZL_OK, 0)
+    mixed = synth.grid_tiles(0, L, L, 3, 1, 2, H) + synth.grid_tiles(1, 10, 10, 1, 2)
+    st, nbytes = _ws(lib, cu, mixed, H)
+    assert st == _lib.ZL_OK and nbytes >= 2 * 10 * H * 64 * 4 + 2 * H * 10 * 4
+    assert nbytes < 2 * L * H * 64 * 4
 
 
 def test_workspace_size_matches_layout(lib):

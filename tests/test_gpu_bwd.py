@@ -64,13 +64,15 @@ def test_cross_lengths_and_keys_without_queries():
     assert torch.all(grads[1][200:330] == 0) and torch.all(grads[2][200:330] == 0)
 
 
-def test_tiles_equal_whole():
+@pytest.mark.parametrize("n_q,n_kv,n_h", [(3, 2, 1), (2, 2, 2), (1, 1, 2)])
+def test_tiles_equal_whole(n_q, n_kv, n_h):
     """The backward of a split sequence sums its tiles' contributions, which is
-    the backward of the whole sequence."""
+    the backward of the whole sequence, for query, key and head splits
+    (the (q, h, k) configurations of the Zellige paper, §IV-A)."""
     wl = synth.Workload("split", [700, 90, 300], 2, 128)
     inp = synth.make_inputs(wl, seed=8, device="cuda")
     cu = wl.cu_seqlens()
-    tiles = synth.grid_tiles(0, 700, 700, 3, 2)
+    tiles = synth.grid_tiles(0, 700, 700, n_q, n_kv, n_h, 2)
     g_t = _fwd_bwd(inp["q"], inp["k"], inp["v"], inp["do"], cu, cu, tiles)
     g_w = _fwd_bwd(inp["q"], inp["k"], inp["v"], inp["do"], cu, cu, None)
     for a, b in zip(g_t, g_w):

@@ -105,7 +105,6 @@ def _sampled_check(wl, inp, o, lse, seed=0, n_random=2048, max_heads_long=4):
     cu = wl.cu_seqlens()
     splits = wl.splits
     worst_o = worst_l = 0.0
-    cache = {}
     for s, L in enumerate(wl.seqlens):
         if L == 0:
             continue
@@ -116,7 +115,6 @@ def _sampled_check(wl, inp, o, lse, seed=0, n_random=2048, max_heads_long=4):
             heads = sorted(set([0, wl.num_heads - 1] + list(rng.choice(wl.num_heads, max_heads_long - 2,
                                                                         replace=False))))
         a, b = cu[s], cu[s + 1]
-        key = (L, tuple(rows.tolist()))
         qs = f64(inp["q"][a:b])
         ks = f64(inp["k"][a:b])
         vs = f64(inp["v"][a:b])
@@ -127,7 +125,6 @@ def _sampled_check(wl, inp, o, lse, seed=0, n_random=2048, max_heads_long=4):
             o_ref, l_ref = oracle.attention_rows(qs, ks, vs, cu1, cu1, 0, h, rows)
             worst_o = max(worst_o, float(np.abs(og[rows, h] - o_ref).max()))
             worst_l = max(worst_l, float(np.abs(lg[h, rows] - l_ref).max()))
-        cache[key] = True
     assert worst_o <= TOL_O_BF16, worst_o
     assert worst_l <= TOL_LSE, worst_l
     return worst_o, worst_l
@@ -170,6 +167,67 @@ def test_fig2_mix_sampled():
     inp = synth.make_inputs(wl, seed=0, device="cuda", with_grad_out=False)
     o, lse = _run(inp, wl, wl.tiles())
     _sampled_check(wl, inp, o, lse, n_random=256, max_heads_long=3)
+
+
+HEAD_SPLIT_CASES = [
+    # (seq, n_q, n_kv, n_h) on the tiny batch (lengths 37, 64, 100, 256; 2 heads)
+    [(3, 1, 1, 2)],
+    [(3, 2, 2, 2), (2, 1, 1, 2)],
+    [(3, 1, 3, 2), (0, 2, 1, 2), (1, 1, 2, 1)],
+]
+
+
+def _head_tiles(cases, lens, nh):
+    return [t for s, nq, nk, nhc in cases for t in synth.grid_tiles(s, lens[s], lens[s], nq, nk, nhc, nh)]
+
+
+@pytest.mark.parametrize("case", range(len(HEAD_SPLIT_CASES)))
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_head_sharded_tiles_tiny(case, dtype):
+    """(q, h, k) configurations of the Zellige paper (§IV-A, Table II) as tile
+    tables: query, head and key splits, alone and composed, against the oracle."""
+    wl = synth.config(1)
+    inp = synth.make_inputs(wl, seed=4, device="cuda", dtype=dtype, with_grad_out=False)
+    tiles = _head_tiles(HEAD_SPLIT_CASES[case], wl.seqlens, wl.num_heads)
+    o, lse = _run(inp, wl, tiles)
+    cu = wl.cu_seqlens()
+    tol_o, tol_l = (TOL_O_BF16, TOL_LSE) if dtype == torch.bfloat16 else (TOL_FP32, TOL_FP32)
+    _full_check(inp["q"], inp["k"], inp["v"], cu, cu, o, lse, tol_o, tol_l)
+    if dtype == torch.bfloat16:
+        o2, l2 = zl.varlen_attn_fwd(inp["q"], inp["k"], inp["v"], cu, cu, tiles=tiles, fused_merge=True)
+        zl.sync_check()
+        _full_check(inp["q"], inp["k"], inp["v"], cu, cu, o2, l2, tol_o, tol_l)
+
+
+def test_query_and_head_splits_are_bitwise_whole():
+    """A sequence cut only along queries and heads, (q, h, 1), computes every
+    row over all of its keys in the same order as the whole sequence: no
+    partials, no merge launch, and bit-identical output."""
+    wl = synth.Workload("qh", [3000, 517, 1024], 8, 128)
+    inp = synth.make_inputs(wl, seed=5, device="cuda", with_grad_out=False)
+    cu = wl.cu_seqlens()
+    tiles = synth.grid_tiles(0, 3000, 3000, 3, 1, 4, 8) + synth.grid_tiles(1, 517, 517, 1, 1, 3, 8)
+    assert zl.fwd_workspace_bytes(cu, cu, 8, 128, tiles) == 0
+    o_whole, l_whole = _run(inp, wl, None)
+    n0 = zl.launch_count()
+    o, lse = _run(inp, wl, tiles)
+    assert zl.launch_count() - n0 == 1
+    assert torch.equal(o, o_whole) and torch.equal(lse, l_whole)
+
+
+def test_qhk_mix_sampled():
+    """A training-size batch with a Ulysses-style (1, 4, 1) 720p video, a
+    composed (2, 2, 2) and a (2, 5, 1) 480p video beside whole images."""
+    wl = synth.config(8)
+    inp = synth.make_inputs(wl, seed=0, device="cuda", with_grad_out=False)
+    o, lse = _run(inp, wl, wl.tiles())
+    _sampled_check(wl, inp, o, lse, n_random=512, max_heads_long=3)
+    o_whole, lse_whole = _run(inp, wl, None)
+    cu = wl.cu_seqlens()
+    for s in (0, 2, 3):           # key axis not split: identical bits
+        a, b = cu[s], cu[s + 1]
+        assert torch.equal(o[a:b], o_whole[a:b]) and torch.equal(lse[:, a:b], lse_whole[:, a:b])
+    assert (o - o_whole).abs().max().item() <= TOL_O_BF16
 
 
 def test_sequence_isolation_bitwise():

@@ -186,6 +186,28 @@ def pin_merge_equals_unsplit():
         assert np.abs(lse - lse_ref).max() < 1e-12
 
 
+def pin_head_sharded_configurations():
+    """Every composed configuration (q, h, k) of the Zellige paper (§IV-A,
+    Table II: query split, head split, key split) reproduces unsplit attention
+    of the split sequences, whole sequences beside them untouched (fp64)."""
+    lens = [37, 100, 64]
+    for cfg in [(1, 2, 1), (2, 2, 2), (1, 3, 2), (3, 1, 1), (1, 1, 3), (2, 3, 1), (1, 5, 1)]:
+        nq, nk, nh = cfg[0], cfg[2], cfg[1]
+        q, k, v, cu = _packed(lens, 5, 8, seed=11 + nq + 3 * nh + 7 * nk)
+        o_ref, lse_ref = oracle.varlen_attn_fwd(q, k, v, cu, cu)
+        tiles = (synth.grid_tiles(0, 37, 37, nq, nk, nh, 5) +
+                 synth.grid_tiles(1, 100, 100, nq, nk, nh, 5))
+        covered = sorted((t[0], h) for t in tiles if t[5] == 0 and t[6] == 0
+                         for h in oracle.tile_heads(t, 5))
+        assert covered == [(s, h) for s in (0, 1) for h in range(5)]
+        o, lse = oracle.tiled_attn_fwd(q, k, v, cu, cu, tiles)
+        assert np.abs(o - o_ref).max() < 1e-12, cfg
+        assert np.abs(lse - lse_ref).max() < 1e-12, cfg
+    # a zero-length head range means every head
+    assert oracle.tile_heads((0, 0, 1, 0, 1, 0, 0, 1, 0, 0, 0), 3) == [0, 1, 2]
+    assert oracle.tile_heads((0, 0, 1, 0, 1, 0, 0, 1), 3) == [0, 1, 2]
+
+
 def pin_merge_empty_parts():
     """An empty partial (LSE = -inf) contributes nothing; all-empty stays empty."""
     r = _rng(9)
@@ -290,7 +312,8 @@ def pin_row_helpers():
 
 PINS = [pin_length_one, pin_constant_keys, pin_identical_values,
         pin_two_keys_closed_form, pin_brute_force_tiny, pin_scipy_softmax,
-        pin_merge_equals_unsplit, pin_merge_empty_parts, pin_finite_differences,
+        pin_merge_equals_unsplit, pin_head_sharded_configurations, pin_merge_empty_parts,
+        pin_finite_differences,
         pin_gradient_sums, pin_sequence_isolation_and_order, pin_row_helpers]
 
 
@@ -330,7 +353,7 @@ def test_golden_wan_token_counts():
 
 
 def test_workload_shapes():
-    """Token totals of the five batches (their descriptions list the per-video
+    """Token totals of the batches (their descriptions list the per-video
     latent sizes, e.g. 21 x 30 x 52 = 32,760 for a 480p 81-frame video)."""
     assert synth.video_tokens(81, 480, 832) == 21 * 30 * 52
     assert synth.video_tokens(33, 480, 832) == 9 * 30 * 52
@@ -344,12 +367,15 @@ def test_workload_shapes():
     assert wl7.num_heads == 12 and len(wl7.tiles()) == 12
     assert len(synth.config(4).tiles()) == 16
     assert len(synth.config(5).tiles()) == 4
-    for n in (4, 5):
+    wl8 = synth.config(8)
+    assert wl8.total_tokens == 75600 + 2 * 32760 + 24 * 1024
+    assert len(wl8.tiles()) == 4 + 8 + 10
+    for n in (4, 5, 7, 8):
         wl = synth.config(n)
-        for s, (nq, nk) in wl.splits.items():
+        for s in wl.splits:
             ts = [t for t in wl.tiles() if t[0] == s]
-            covered = sum(t[2] * t[4] for t in ts)
-            assert covered == wl.seqlens[s] ** 2
+            covered = sum(t[2] * t[4] * (t[9] or wl.num_heads) for t in ts)
+            assert covered == wl.seqlens[s] ** 2 * wl.num_heads
 
 
 def test_inputs_seeded():
@@ -435,9 +461,16 @@ def _mut_grad_v_wrong_side(p, do_rows):
     return np.zeros((p.shape[1], do_rows.shape[1]))
 
 
+def _mut_tile_heads_from_zero(tile, num_heads):
+    # drops the head offset: every head chunk reads heads 0 .. h_len-1
+    if len(tile) > 9 and int(tile[9]) > 0:
+        return list(range(int(tile[9])))
+    return list(range(num_heads))
+
+
 _REAL = {name: getattr(of, name) for name in
          ("scores", "row_logsumexp", "probabilities", "lse_merge", "grad_scores",
-          "grad_q", "grad_k", "grad_v")}
+          "grad_q", "grad_k", "grad_v", "tile_heads")}
 
 MUTATIONS = [
     ("scores", _mut_no_scale), ("scores", _mut_inverse_scale),
@@ -447,7 +480,7 @@ MUTATIONS = [
     ("lse_merge", _mut_merge_max_only), ("lse_merge", _mut_merge_unweighted),
     ("grad_scores", _mut_grad_scores_no_d), ("grad_scores", _mut_grad_scores_sign),
     ("grad_q", _mut_grad_q_no_scale), ("grad_k", _mut_grad_k_no_transpose),
-    ("grad_v", _mut_grad_v_wrong_side),
+    ("grad_v", _mut_grad_v_wrong_side), ("tile_heads", _mut_tile_heads_from_zero),
 ]
 
 

@@ -9,29 +9,32 @@
 // in shared memory and the dV / dK accumulators in TMEM, and walks every
 // 64-row query block i of the sequence (starting at a block that depends on
 // j, so CTAs working on one head spread their dQ additions over different
-// rows).  Key rows sit on the 128 TMEM lanes.  Per query block, in one of two
-// alternating TMEM buffers b:
-//     S^T  = K_j Q_i^T      (SS MMA, N = 64)           -> S[b]
-//     dP^T = V_j dO_i^T     (SS MMA)                   -> DP[b]
-//     softmax-grad warps: P^T = 2^(S^T*scale*log2e - LSE*log2e) and
-//       dS^T = P^T (dP^T - D) in bf16, written over S[b] / DP[b] for the TS
-//       MMAs, and dS into shared memory as an MN-major operand
+// rows).  Key rows sit on the 128 TMEM lanes.  Per query block g:
+//     S^T  = K_j Q_i^T      (SS MMA, N = 64)           -> S[g % 2]
+//     dP^T = V_j dO_i^T     (SS MMA)                   -> DP
+//     softmax-grad warps load S^T and dP^T (DP is then free for the next
+//       block), form P^T = 2^(S^T*scale*log2e - LSE*log2e) in bf16 over
+//       S[g % 2] for the TS MMA, and dS^T = P^T (dP^T - D) in bf16 into shared
+//       memory ([key][query], the operand layout both MMAs below read)
 //     dV  += P^T dO_i       (TS MMA, A from TMEM)      -> TMEM
-//     dK  += dS^T Q_i       (TS MMA)                   -> TMEM
-//     dQ_i^T = K_j^T dS_i^T (SS MMA, both MN-major)    -> S[b] (d on the lanes)
+//     dK  += dS^T Q_i       (SS MMA, A = dS^T K-major) -> TMEM
+//     dQ_i^T = K_j^T dS_i^T (SS MMA, both MN-major)    -> DQ (d on the lanes)
 //     drain warps read dQ_i^T out of TMEM, stage it in 128-byte-swizzled
-//       32-column boxes inside the now dead Q_i/dO_i stage, and add it into a
-//       float32 accumulator in global memory with TMA reduce-add (a bulk copy
-//       holds no load/store slots while L2 performs the additions); the stage
-//       goes back to the producer once the copy engine has read it.
-//       dq_convert later scales and rounds the accumulator.
+//       32-column boxes inside the Q_i/dO_i stage once dV and dK are done
+//       with it, and add it into a float32 accumulator in global memory with
+//       TMA reduce-add (a bulk copy holds no load/store slots while L2
+//       performs the additions); the stage goes back to the producer once the
+//       copy engine has read it.  dq_convert later scales and rounds it.
+// dQ^T has a TMEM region of its own, so the chain dQ^T -> drain runs beside
+// the main loop: S^T of block g+2 reuses S[g % 2] right after dV of block g
+// (issued earlier by the same thread, and MMAs of one thread execute in
+// order), and dP^T of block g+1 reuses DP once the softmax-grad warps have
+// loaded dP^T of block g.
 // Each query block's MMAs come from three issuing threads in different warps
 // (one thread issues a tcgen05.mma only every ~70-95 cycles, and the N = 64
-// MMAs here take 32-64 cycles of tensor time each): A issues S^T and dV
-// (everything on S[b]), B issues dP^T and dK (everything on DP[b]), C issues
-// dQ^T once dV has read P^T out of S[b].  A and B issue their (S^T or dP^T)
-// for two query blocks and then the two accumulations, so the softmax-grad of
-// one block overlaps the tensor work of the other.
+// MMAs here take 32-64 cycles of tensor time each): A issues S^T and dV,
+// B issues dP^T and dK, C issues dQ^T.  A and B issue the S^T / dP^T of the
+// next block before the accumulation of the current one.
 //
 // Roles (512 threads, one CTA per SM): warps 0-7 softmax-grad (warp w reads
 // TMEM lanes 32*(w%4).. and query columns 32*(w/4)..) and the dV/dK epilogue,
@@ -68,7 +71,9 @@ struct BwdSmem {
   float dsum[2][kBQ];                             // D of the query block
   uint64_t kv_full, kv_empty;
   uint64_t qd_full[kQdStages], qd_empty[kQdStages];
-  uint64_t s_full[2], sg_done[2], dv_done[2], dk_done[2], dq_full[2], dq_drained[2];
+  uint64_t qd_read[kQdStages];                    // dV and dK of the stage's block are done
+  uint64_t s_full[2], sg_done[2], ds_free[2];
+  uint64_t dp_free, dq_full, dq_drained;
   uint64_t stage_full, dkdv_full, dkdv_drained;
   uint32_t tmem_base;
   int abort_flag;
@@ -131,15 +136,16 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     for (int s = 0; s < kQdStages; ++s) {
       mbar_init(&sm->qd_full[s], 1);
       mbar_init(&sm->qd_empty[s], kDrainThreads / 32);   // each drain warp, after its reduce read the stage
+      mbar_init(&sm->qd_read[s], 2);                     // dV (A) and dK (B) commits
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm->s_full[b], 2);                // S^T from A, dP^T from B
       mbar_init(&sm->sg_done[b], kSgThreads);
-      mbar_init(&sm->dv_done[b], 1);
-      mbar_init(&sm->dk_done[b], 1);
-      mbar_init(&sm->dq_full[b], 1);
-      mbar_init(&sm->dq_drained[b], kDrainThreads);
+      mbar_init(&sm->ds_free[b], 2);               // dK (B) and dQ^T (C) have read dS
     }
+    mbar_init(&sm->dp_free, kSgThreads);
+    mbar_init(&sm->dq_full, 1);
+    mbar_init(&sm->dq_drained, kDrainThreads);
     mbar_init(&sm->stage_full, kSgThreads);
     mbar_init(&sm->dkdv_full, 2);
     mbar_init(&sm->dkdv_drained, kSgThreads);
@@ -154,7 +160,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
-  // S[b] = tmem + 64b, DP[b] = tmem + 128 + 64b (64 columns each), dV, dK.
+  // S[b] = tmem + 64b, DP = tmem + 128, DQ = tmem + 192 (64 columns each), dV, dK.
+  const uint32_t tDP = tmem + 128;
+  const uint32_t tDQ = tmem + 192;
   const uint32_t tDV = tmem + 256;
   const uint32_t tDK = tmem + 384;
 
@@ -202,87 +210,93 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
   } else if (warp == kMmaWarpA || warp == kMmaWarpB) {
     // ------------------------------------------------------------ MMA issuers A and B
-    // A: S^T_i = K Q_i^T -> S[b], then dV += P^T dO_i (P^T read from S[b]).
-    // B: dP^T_i = V dO_i^T -> DP[b], then dK += dS^T Q_i (dS^T from DP[b]).
-    // Each issues (S^T or dP^T) for two query blocks, then the two
-    // accumulations, so softmax-grad of one block overlaps the MMAs of the other.
+    // A: S^T_g = K Q_g^T -> S[g % 2], then dV += P^T dO_g (P^T read from S[g % 2]).
+    // B: dP^T_g = V dO_g^T -> DP, then dK += dS^T Q_g (dS^T read from shared memory).
+    // Each issues the S^T (or dP^T) of block g+1 before the accumulation of
+    // block g, so the softmax-grad of g+1 can start while g accumulates.
     if (lane == 0) {
       const bool is_a = warp == kMmaWarpA;
       constexpr uint32_t idesc_s = idesc_bf16(kBlockN, kBQ, false, false);   // M128 N64
       constexpr uint32_t idesc_acc = idesc_bf16(kBlockN, HD, false, true);   // dV, dK
       const uint32_t a_op = smem_u32(is_a ? sm->k : sm->v);                   // K for S^T, V for dP^T
-      const uint32_t t_acc = is_a ? tDV : tDK;
       const uint32_t err = ERR_TIMEOUT_MMA;
-      uint32_t item_it = 0, g = 0;
+      uint32_t item_it = 0, g0 = 0;
       bool ok = true;
+      // S^T (A) or dP^T (B) of block gg into S[gg % 2] or DP.
+      auto issue_first = [&](uint32_t gg) -> bool {
+        const uint32_t b = gg & 1u;
+        const uint32_t st = gg % kQdStages;
+        if (!mbar_wait(&sm->qd_full[st], (gg / kQdStages) & 1u, abort_flag, &g_bwd_err, err)) return false;
+        // B: the softmax-grad warps must have loaded dP^T of block gg-1
+        if (!is_a && gg > 0 && !mbar_wait(&sm->dp_free, (gg - 1) & 1u, abort_flag, &g_bwd_err, err)) return false;
+        tc_fence_after();
+        const uint32_t b_op = smem_u32(sm->qd[st]) + (is_a ? 0u : static_cast<uint32_t>(kBQ * HD * 2));
+        const uint32_t t_out = is_a ? tmem + 64u * b : tDP;
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks) {
+          const uint32_t ka = (ks >> 2) * (kBlockN * 128) + (ks & 3) * 32;
+          const uint32_t qa = (ks >> 2) * (kBQ * 128) + (ks & 3) * 32;
+          umma_ss(t_out, sdesc_sw128(a_op + ka, 16, 1024), sdesc_sw128(b_op + qa, 16, 1024), idesc_s,
+                  ks > 0 ? 1u : 0u);
+        }
+        umma_commit(&sm->s_full[b]);
+        return true;
+      };
       for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x, ++item_it) {
         const BwdWork w = decode_bwd(args, it);
         const BwdSeg& sg = args.segs[w.seg];
-        const int nqb = (sg.q_len + kBQ - 1) / kBQ;
-        if (!mbar_wait(&sm->kv_full, item_it & 1u, abort_flag, &g_bwd_err, err)) {
+        const uint32_t nqb = static_cast<uint32_t>((sg.q_len + kBQ - 1) / kBQ);
+        if (!mbar_wait(&sm->kv_full, item_it & 1u, abort_flag, &g_bwd_err, err) || !issue_first(g0)) {
           ok = false;
           break;
         }
-        for (int i0 = 0; i0 < nqb && ok; i0 += 2) {
-          const int n_in = nqb - i0 < 2 ? nqb - i0 : 2;
-          for (int u = 0; u < n_in; ++u) {
-            const uint32_t gg = g + i0 + u;
-            const uint32_t b = gg & 1u;
-            const uint32_t st = gg % kQdStages;
-            // A must also wait until dQ^T of block gg-2 has left S[b]
-            if (!mbar_wait(&sm->qd_full[st], (gg / kQdStages) & 1u, abort_flag, &g_bwd_err, err) ||
-                (is_a && !mbar_wait(&sm->dq_drained[b], ((gg >> 1) & 1u) ^ 1u, abort_flag, &g_bwd_err, err))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            // B operand: Q_i for S^T, dO_i for dP^T
-            const uint32_t b_op = smem_u32(sm->qd[st]) + (is_a ? 0u : static_cast<uint32_t>(kBQ * HD * 2));
-            const uint32_t t_out = tmem + (is_a ? 0u : 128u) + 64u * b;
-#pragma unroll
-            for (int ks = 0; ks < HD / 16; ++ks) {
-              const uint32_t ka = (ks >> 2) * (kBlockN * 128) + (ks & 3) * 32;
-              const uint32_t qa = (ks >> 2) * (kBQ * 128) + (ks & 3) * 32;
-              umma_ss(t_out, sdesc_sw128(a_op + ka, 16, 1024), sdesc_sw128(b_op + qa, 16, 1024), idesc_s,
-                      ks > 0 ? 1u : 0u);
-            }
-            umma_commit(&sm->s_full[b]);
+        for (uint32_t ii = 0; ii < nqb; ++ii) {
+          const uint32_t gg = g0 + ii;
+          const uint32_t b = gg & 1u;
+          const uint32_t st = gg % kQdStages;
+          if (ii + 1 < nqb && !issue_first(gg + 1)) {
+            ok = false;
+            break;
           }
-          if (!ok) break;
-          for (int u = 0; u < n_in; ++u) {
-            const int ii = i0 + u;
-            const uint32_t gg = g + ii;
-            const uint32_t b = gg & 1u;
-            const uint32_t st = gg % kQdStages;
-            if (!mbar_wait(&sm->sg_done[b], (gg >> 1) & 1u, abort_flag, &g_bwd_err, err) ||
-                (ii == 0 && !mbar_wait(&sm->dkdv_drained, (item_it & 1u) ^ 1u, abort_flag, &g_bwd_err, err))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            // dV: B = dO_i (MN-major); dK: B = Q_i (MN-major)
-            const uint32_t b_op = smem_u32(sm->qd[st]) + (is_a ? static_cast<uint32_t>(kBQ * HD * 2) : 0u);
-            const uint32_t t_a = tmem + (is_a ? 0u : 128u) + 64u * b;
-            const uint32_t acc0 = ii > 0 ? 1u : 0u;
+          if (!mbar_wait(&sm->sg_done[b], (gg >> 1) & 1u, abort_flag, &g_bwd_err, err) ||
+              (ii == 0 && !mbar_wait(&sm->dkdv_drained, (item_it & 1u) ^ 1u, abort_flag, &g_bwd_err, err))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t acc0 = ii > 0 ? 1u : 0u;
+          if (is_a) {
+            // dV: A = P^T in S[b] (TMEM), B = dO_g (MN-major)
+            const uint32_t do_op = smem_u32(sm->qd[st]) + static_cast<uint32_t>(kBQ * HD * 2);
 #pragma unroll
             for (int ks = 0; ks < kBQ / 16; ++ks) {
-              umma_ts(t_acc, t_a + op_col(ks), sdesc_sw128(b_op + ks * 2048, kBQ * 128, 1024), idesc_acc,
-                      acc0 | (ks > 0 ? 1u : 0u));
+              umma_ts(tDV, tmem + 64u * b + op_col(ks), sdesc_sw128(do_op + ks * 2048, kBQ * 128, 1024),
+                      idesc_acc, acc0 | (ks > 0 ? 1u : 0u));
             }
-            umma_commit(is_a ? &sm->dv_done[b] : &sm->dk_done[b]);
+          } else {
+            // dK: A = dS^T as [key][query] rows (K-major), B = Q_g (MN-major)
+            const uint32_t ds_op = smem_u32(sm->ds[b]);
+            const uint32_t q_op = smem_u32(sm->qd[st]);
+#pragma unroll
+            for (int ks = 0; ks < kBQ / 16; ++ks) {
+              umma_ss(tDK, sdesc_sw128(ds_op + ks * 32, 16, 1024), sdesc_sw128(q_op + ks * 2048, kBQ * 128, 1024),
+                      idesc_acc, acc0 | (ks > 0 ? 1u : 0u));
+            }
+            umma_commit(&sm->ds_free[b]);
           }
+          umma_commit(&sm->qd_read[st]);
         }
         if (!ok) break;
-        g += nqb;
+        g0 += nqb;
         umma_commit(&sm->dkdv_full);
         umma_commit(&sm->kv_empty);
       }
     }
   } else if (warp == kMmaWarpC) {
     // ------------------------------------------------------------ MMA issuer C
-    // dQ_i^T = K^T dS_i^T into S[b] once dV has read P^T out of it.  A = K as
-    // MN-major (d on M; for d = 64 the upper 64 rows read the V tile and are
-    // never drained), B = dS MN-major.
+    // dQ_g^T = K^T dS_g^T into DQ once the drain warps have read the previous
+    // block's dQ^T out of it.  A = K as MN-major (d on M; for d = 64 the upper
+    // 64 rows read the V tile and are never drained), B = dS MN-major.
     if (lane == 0) {
       constexpr uint32_t idesc_dq = idesc_bf16(128, kBQ, true, true);        // M128 N64
       const uint32_t k_addr = smem_u32(sm->k);
@@ -296,11 +310,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           ok = false;
           break;
         }
-        for (int ii = 0; ii < nqb; ++ii) {
-          const uint32_t gg = g + ii;
-          const uint32_t b = gg & 1u;
-          if (!mbar_wait(&sm->sg_done[b], (gg >> 1) & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA) ||
-              !mbar_wait(&sm->dv_done[b], (gg >> 1) & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA)) {
+        for (int ii = 0; ii < nqb; ++ii, ++g) {
+          const uint32_t b = g & 1u;
+          if (!mbar_wait(&sm->sg_done[b], (g >> 1) & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA) ||
+              (g > 0 && !mbar_wait(&sm->dq_drained, (g - 1) & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA))) {
             ok = false;
             break;
           }
@@ -308,13 +321,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           const uint32_t ds_addr = smem_u32(sm->ds[b]);
 #pragma unroll
           for (int ks = 0; ks < kBlockN / 16; ++ks) {
-            umma_ss(tmem + 64 * b, sdesc_sw128(k_addr + ks * 2048, kBlockN * 128, 1024),
+            umma_ss(tDQ, sdesc_sw128(k_addr + ks * 2048, kBlockN * 128, 1024),
                     sdesc_sw128(ds_addr + ks * 2048, 16, 1024), idesc_dq, ks > 0 ? 1u : 0u);
           }
-          umma_commit(&sm->dq_full[b]);
+          umma_commit(&sm->dq_full);
+          umma_commit(&sm->ds_free[b]);
         }
         if (!ok) break;
-        g += nqb;
         umma_commit(&sm->kv_empty);
       }
     }
@@ -334,29 +347,28 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const int start = w.kb % nqb;
       for (int ii = 0; ii < nqb; ++ii, ++g) {
         const int i = (start + ii) % nqb;
-        const uint32_t b = g & 1u;
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(&sm->dq_full[b], (g >> 1) & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_OTHER))) {
+                        mbar_wait(&sm->dq_full, g & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_OTHER))) {
           ok = false;
           break;
         }
         tc_fence_after();
         uint32_t v0[32], v1[32];
-        tmem_ld32(tmem + 64 * b + lane_off, v0);
-        tmem_ld32(tmem + 64 * b + lane_off + 32, v1);
+        tmem_ld32(tDQ + lane_off, v0);
+        tmem_ld32(tDQ + lane_off + 32, v1);
         tmem_wait_ld();
         reg_fence(v0);
         reg_fence(v1);
         tc_fence_before();
-        mbar_arrive(&sm->dq_drained[b]);
+        mbar_arrive(&sm->dq_drained);
         const uint32_t st = g % kQdStages;
         if (!active) {
           if (lane == 0) mbar_arrive(&sm->qd_empty[st]);
           continue;
         }
-        // dK (issuer B) may still be reading Q_i out of this stage
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(&sm->dk_done[b], (g >> 1) & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_OTHER))) {
+        // dV and dK (issuers A, B) may still be reading dO_i / Q_i out of this stage
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm->qd_read[st], (g / kQdStages) & 1u, abort_flag, &g_bwd_err,
+                                               ERR_TIMEOUT_OTHER))) {
           ok = false;
           break;
         }
@@ -408,22 +420,20 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (!__all_sync(0xffffffffu,
                         mbar_wait(&sm->stage_full, g & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_SOFTMAX)) ||
             !__all_sync(0xffffffffu,
-                        mbar_wait(&sm->s_full[b], (g >> 1) & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_SOFTMAX)) ||
-            !__all_sync(0xffffffffu,
-                        g < 2 || mbar_wait(&sm->dq_full[b], ((g - 2) >> 1) & 1u, abort_flag, &g_bwd_err,
-                                           ERR_TIMEOUT_SOFTMAX))) {
+                        mbar_wait(&sm->s_full[b], (g >> 1) & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_SOFTMAX))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t tS = tmem + 64 * b + lane_off + 32 * half;
-        const uint32_t tDP = tmem + 128 + 64 * b + lane_off + 32 * half;
         uint32_t s[32], dp[32];
         tmem_ld32(tS, s);
-        tmem_ld32(tDP, dp);
+        tmem_ld32(tDP + lane_off + 32 * half, dp);
         tmem_wait_ld();
         reg_fence(s);
         reg_fence(dp);
+        tc_fence_before();
+        mbar_arrive(&sm->dp_free);             // dP^T of the next block may overwrite DP
         const float* l2 = sm->lse2[b] + 32 * half;
         const float* dsm = sm->dsum[b] + 32 * half;
         uint32_t pp[16], dd[16];
@@ -443,7 +453,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           dd[e] = pack_bf16x2(d0, d1);
         }
         tmem_st16(tS, pp);
-        tmem_st16(tDP, dd);
+        // dS of block g-2 must have been read by dK and dQ^T before it is overwritten
+        if (!__all_sync(0xffffffffu, g < 2 || mbar_wait(&sm->ds_free[b], ((g - 2) >> 1) & 1u, abort_flag,
+                                                         &g_bwd_err, ERR_TIMEOUT_SOFTMAX))) {
+          ok = false;
+          break;
+        }
         uint8_t* ds_row = sm->ds[b] + jrow * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {

@@ -279,11 +279,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          mx0 = fmaxf(mx0, __uint_as_float(s[0][i]));
-          mx1 = fmaxf(mx1, __uint_as_float(s[1][i]));
-          mx2 = fmaxf(mx2, __uint_as_float(s[2][i]));
-          mx3 = fmaxf(mx3, __uint_as_float(s[3][i]));
+        for (int i = 0; i < 32; i += 2) {
+          mx0 = fmax3(mx0, __uint_as_float(s[0][i]), __uint_as_float(s[0][i + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(s[1][i]), __uint_as_float(s[1][i + 1]));
+          mx2 = fmax3(mx2, __uint_as_float(s[2][i]), __uint_as_float(s[2][i + 1]));
+          mx3 = fmax3(mx3, __uint_as_float(s[3][i]), __uint_as_float(s[3][i + 1]));
         }
         const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
         const float m_new = fmaxf(m_run, m_blk);
@@ -295,21 +295,33 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         l_run *= alpha;
         const float neg_m = -m_run;
-        float ls0 = 0.f, ls1 = 0.f;
-        uint32_t p[2][32];
+        // exponent arguments and row sums on float32 pairs; each half of P
+        // goes to TMEM as soon as it is packed, freeing its S registers
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        const uint64_t negm2 = f2_pack(neg_m, neg_m);
+        uint64_t acc[2] = {0ull, 0ull};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t p[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a = fast_exp2(fmaf(__uint_as_float(s[c][2 * i]), sl2, neg_m));
-            const float b = fast_exp2(fmaf(__uint_as_float(s[c][2 * i + 1]), sl2, neg_m));
-            ls0 += a;
-            ls1 += b;
-            p[c >> 1][(c & 1) * 16 + i] = pack_bf16x2(a, b);
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * hf + cc;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint64_t t = f2_fma(f2_pack(__uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1])),
+                                        sl2x2, negm2);
+              float t0, t1;
+              f2_unpack(t, t0, t1);
+              const float a = fast_exp2(t0);
+              const float b = fast_exp2(t1);
+              acc[i & 1] = f2_add(acc[i & 1], f2_pack(a, b));
+              p[cc * 16 + i] = pack_bf16x2(a, b);
+            }
           }
+          tmem_st32(tS + lane_off + 32 * hf, p);
         }
-        tmem_st32(tS + lane_off + 0, p[0]);
-        tmem_st32(tS + lane_off + 32, p[1]);
+        float ls0, ls1;
+        f2_unpack(f2_add(acc[0], acc[1]), ls0, ls1);
         if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
           for (int c = 0; c < HD / 32; ++c) {

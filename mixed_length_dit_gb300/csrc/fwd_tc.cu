@@ -1,32 +1,41 @@
 // Forward of coalesced varlen attention on sm_103a tensor cores.
 //
 // One persistent launch runs every work item of the batch: a work item is
-// (segment, head, 128-row query block), where a segment is a whole sequence
-// or one (query-chunk x KV-chunk) shard tile of a split sequence (Zellige,
-// arXiv 2608.01150v1, §IV-D: whole sequences packed into one block-diagonal
-// call, shards alongside them).  Items arrive ordered longest-first from the
-// host scheduler and are taken in a static stride by the CTAs.
+// (segment, head, pair of 128-row query tiles), where a segment is a whole
+// sequence or one shard tile of a split sequence (Zellige, arXiv
+// 2608.01150v1, §IV-D: whole sequences packed into one block-diagonal call,
+// shards alongside them).  Items arrive ordered longest-first from the host
+// scheduler and are taken in a static stride by the CTAs, one CTA per SM.
 //
-// Per CTA (192 threads, two CTAs per SM):
-//   warp 4     TMA producer: Q tile once per item, then K_j / V_j tiles
-//              through a two-stage ring (128-byte swizzle, 64-column boxes).
-//   warp 5     MMA issuer (one thread):  S = Q K_j^T  (SS, M=128 N=128) into
-//              TMEM, then O += P V_j  (TS: P read from TMEM, V from shared
-//              memory as an MN-major operand) into TMEM.
-//   warps 0-3  softmax: thread t owns query row t = TMEM lane t.  Loads its S
-//              row, tracks the running max m and sum l in base 2, writes
-//              P = 2^(S*scale*log2e - m) as bf16 over the S columns, and
-//              rescales the O row in TMEM when m grows by more than 2^8
-//              (lazy rescale; exactness holds for any m used consistently).
-//              After the last block it normalises O and writes O and LSE.
-// TMEM: S/P in columns [0,128), O in [128, 128+d); 256 columns per CTA.
+// The two query tiles of an item share every K_j / V_j tile that the producer
+// brings into shared memory.  Per CTA (352 threads):
+//   warp 8      TMA producer: the two Q tiles once per item, then K_j / V_j
+//               through a four-stage ring (128-byte swizzle, 64-column boxes).
+//   warps 9,10  MMA issuers, one thread each, one per query tile t:
+//               S_t = Q_t K_j^T (SS, M=128 N=128) into TMEM, then
+//               O_t += P_t V_j (TS: P read from TMEM, V from shared memory as
+//               an MN-major operand) into TMEM.  One issuing thread per tile,
+//               because a thread issues a tcgen05.mma only every ~70-95 cycles.
+//   warps 0-7   softmax, warpgroup t for tile t: thread r of the group owns
+//               query row r = TMEM lane r.  Loads its S row, tracks the
+//               running max m and sum l in base 2, writes
+//               P = 2^(S*scale*log2e - m) as bf16 over the S columns, and
+//               rescales the O row in TMEM when m grows by more than 2^8
+//               (lazy rescale; exactness holds for any m used consistently).
+//               After the last block it normalises O and writes O and LSE.
+//   The two warpgroups take turns (an mbarrier per group, handed back and
+//   forth): the exponentials of one tile run while the tensor cores work on
+//   the other tile, instead of both groups competing for the SFU while the
+//   tensor pipe idles.
+// TMEM: tile t uses S/P in columns [256t, 256t+128) and O in
+// [256t+128, 256t+128+d); 512 columns.
 //
 // Whole sequences write O in bf16 and LSE in natural log.  Tiles write float32
 // partial O and their own LSE into a partial slot for the merge kernel; with
 // the fused merge they then count themselves in an arrival counter per
-// (query block, head) of their query chunk, and the CTA that brings the count
-// to the number of kv chunks merges all partials of those 128 rows into O and
-// LSE exactly (no waiting: every other partial is complete and fenced by then).
+// (query block, head) of their query chunk, and the warpgroup that brings the
+// count to the number of kv chunks merges all partials of those 128 rows into
+// O and LSE exactly (no waiting: every other partial is complete and fenced).
 #include "common.cuh"
 #include "launch.h"
 #include "work.cuh"
@@ -36,24 +45,25 @@ namespace {
 
 __device__ uint32_t g_fwd_err;
 
-constexpr int kFwdThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kFwdStages = 2;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kFwdThreads = 352;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp0 = 9;                 // tile 0; tile 1 is kMmaWarp0 + 1
+constexpr int kFwdStages = 4;
+constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // in log2 units: P <= 2^8
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int HD>
 struct FwdSmem {
-  uint8_t q[kBlockM * HD * 2];                 // HD/64 boxes of [128 rows][128 B]
+  uint8_t q[2][kBlockM * HD * 2];              // per tile: HD/64 boxes of [128 rows][128 B]
   uint8_t kv[kFwdStages][kBlockN * HD * 2];    // K_j or V_j, same box layout
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[kFwdStages], kv_empty[kFwdStages];
-  uint64_t s_full, p_full, o_full;
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t turn[2];                            // softmax group t may run its next block
   uint32_t tmem_base;
   int abort_flag;
-  int is_last;                                 // this CTA completed a tile row block's partials
+  int is_last[2];                              // group t completed a row block's partials
 };
 
 // Merges the n_kv float32 partials of one query row of a tile (all written
@@ -106,8 +116,15 @@ __device__ __forceinline__ void drain_delay(uint64_t ns) {
   }
 }
 
+// Does query tile t (0 or 1) of this item hold any row of the segment?
+__device__ __forceinline__ bool tile_present(const FwdSeg& sg, const FwdWork& w, int t) {
+  return (2 * w.qb + t) * kBlockM < sg.q_len;
+}
+
+// Registers are granted per group of four warps, so 352 threads leave at
+// most 168 registers per thread.
 template <int HD>
-__global__ void __launch_bounds__(kFwdThreads, 2)
+__global__ void __launch_bounds__(kFwdThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdArgs args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -118,19 +135,22 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   volatile int* abort_flag = &sm->abort_flag;
 
   if (threadIdx.x == 0) {
-    mbar_init(&sm->q_full, 1);
-    mbar_init(&sm->q_empty, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm->q_full[t], 1);
+      mbar_init(&sm->q_empty[t], 1);
+      mbar_init(&sm->s_full[t], 1);
+      mbar_init(&sm->p_full[t], 128);
+      mbar_init(&sm->o_full[t], 1);
+      mbar_init(&sm->turn[t], 128);
+    }
     for (int s = 0; s < kFwdStages; ++s) {
       mbar_init(&sm->kv_full[s], 1);
-      mbar_init(&sm->kv_empty[s], 1);
+      mbar_init(&sm->kv_empty[s], 2);          // both issuers are done with the stage
     }
-    mbar_init(&sm->s_full, 1);
-    mbar_init(&sm->p_full, 128);
-    mbar_init(&sm->o_full, 1);
     sm->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp0) {
     tmem_alloc(&sm->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -138,38 +158,39 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
-  const uint32_t tS = tmem;          // S (f32) / P (bf16 pairs) columns [0,128)
-  const uint32_t tO = tmem + 128;    // O (f32) columns [128, 128+HD)
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
-      uint32_t kv_it = 0, item_it = 0;
+      uint32_t kv_it = 0;
+      uint32_t q_it[2] = {0u, 0u};
       bool ok = true;
-      for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x, ++item_it) {
+      for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x) {
         const FwdWork w = decode_fwd(args, it);
         const FwdSeg& sg = args.segs[w.seg];
-        const int q_row = sg.q_row0 + w.qb * kBlockM;
         const int nkb = (sg.k_len + kBlockN - 1) / kBlockN;
         const int x0 = w.h * HD;
-        if (!mbar_wait(&sm->q_empty, (item_it & 1u) ^ 1u, abort_flag, &g_fwd_err,
-                       ERR_TIMEOUT_PRODUCER)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&sm->q_full, kBlockM * HD * 2);
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!tile_present(sg, w, t)) continue;
+          if (!mbar_wait(&sm->q_empty[t], (q_it[t] & 1u) ^ 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          ++q_it[t];
+          mbar_arrive_expect_tx(&sm->q_full[t], kBlockM * HD * 2);
+          const int q_row = sg.q_row0 + (2 * w.qb + t) * kBlockM;
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c)
-          tma_load_2d(sm->q + c * kBlockM * 128, &tmQ, &sm->q_full, x0 + c * 64, q_row);
+          for (int c = 0; c < HD / 64; ++c)
+            tma_load_2d(sm->q[t] + c * kBlockM * 128, &tmQ, &sm->q_full[t], x0 + c * 64, q_row);
+        }
         for (int j = 0; j < nkb && ok; ++j) {
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
             const uint32_t st = kv_it % kFwdStages;
             const uint32_t ph = (kv_it / kFwdStages) & 1u;
-            if (!mbar_wait(&sm->kv_empty[st], ph ^ 1u, abort_flag, &g_fwd_err,
-                           ERR_TIMEOUT_PRODUCER)) {
+            if (!mbar_wait(&sm->kv_empty[st], ph ^ 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_PRODUCER)) {
               ok = false;
               break;
             }
@@ -184,23 +205,31 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
+    // ------------------------------------------------------------ MMA issuer of tile t
+    // Every K/V stage is released by both issuers, also by the issuer of an
+    // absent tile 1 (which waits for each stage to fill, so it can never
+    // release a stage twice within one fill).
     if (lane == 0) {
+      const int t = warp - kMmaWarp0;
       constexpr uint32_t idesc_qk = idesc_bf16(kBlockM, kBlockN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(kBlockM, HD, false, true);
-      const uint32_t q_addr = smem_u32(sm->q);
-      uint32_t kv_it = 0, item_it = 0, blk_it = 0;
+      const uint32_t q_addr = smem_u32(sm->q[t]);
+      const uint32_t tS = tmem + 256u * t;
+      const uint32_t tO = tS + 128u;
+      uint32_t kv_it = 0, q_it = 0, blk_it = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x, ++item_it) {
+      for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x) {
         const FwdWork w = decode_fwd(args, it);
         const FwdSeg& sg = args.segs[w.seg];
         const int nkb = (sg.k_len + kBlockN - 1) / kBlockN;
-        if (!mbar_wait(&sm->q_full, item_it & 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_MMA)) {
+        const bool has = tile_present(sg, w, t);
+        if (has && !mbar_wait(&sm->q_full[t], q_it & 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_MMA)) {
           ok = false;
           break;
         }
-        for (int j = 0; j < nkb; ++j, ++blk_it) {
-          // S = Q K_j^T
+        for (int j = 0; j < nkb; ++j) {
+          // S_t = Q_t K_j^T
           uint32_t st = kv_it % kFwdStages;
           uint32_t ph = (kv_it / kFwdStages) & 1u;
           if (!mbar_wait(&sm->kv_full[st], ph, abort_flag, &g_fwd_err, ERR_TIMEOUT_MMA)) {
@@ -208,59 +237,81 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             break;
           }
           tc_fence_after();
-          const uint32_t k_addr = smem_u32(sm->kv[st]);
+          if (has) {
+            const uint32_t k_addr = smem_u32(sm->kv[st]);
 #pragma unroll
-          for (int ks = 0; ks < HD / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * (kBlockM * 128) + (ks & 3) * 32;
-            umma_ss(tS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                    idesc_qk, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < HD / 16; ++ks) {
+              const uint32_t off = (ks >> 2) * (kBlockM * 128) + (ks & 3) * 32;
+              umma_ss(tS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+                      idesc_qk, ks > 0 ? 1u : 0u);
+            }
+            umma_commit(&sm->s_full[t]);
+            // Q_t is read by S MMAs only: after the item's last one the
+            // producer may bring the next item's Q_t
+            if (j == nkb - 1) umma_commit(&sm->q_empty[t]);
           }
-          umma_commit(&sm->s_full);
           umma_commit(&sm->kv_empty[st]);
-          if (j == nkb - 1) umma_commit(&sm->q_empty);
           ++kv_it;
-          // O += P V_j once the softmax warps have written P_j (and rescaled O)
+          // O_t += P_t V_j once softmax group t has written P_t (and rescaled O_t)
           st = kv_it % kFwdStages;
           ph = (kv_it / kFwdStages) & 1u;
           if (!mbar_wait(&sm->kv_full[st], ph, abort_flag, &g_fwd_err, ERR_TIMEOUT_MMA) ||
-              !mbar_wait(&sm->p_full, blk_it & 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_MMA)) {
+              (has && !mbar_wait(&sm->p_full[t], blk_it & 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_MMA))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t v_addr = smem_u32(sm->kv[st]);
+          if (has) {
+            const uint32_t v_addr = smem_u32(sm->kv[st]);
 #pragma unroll
-          for (int ks = 0; ks < kBlockN / 16; ++ks) {
-            umma_ts(tO, tS + ks * 8, sdesc_sw128(v_addr + ks * 2048, kBlockN * 128, 1024),
-                    idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < kBlockN / 16; ++ks) {
+              umma_ts(tO, tS + ks * 8, sdesc_sw128(v_addr + ks * 2048, kBlockN * 128, 1024),
+                      idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+            }
+            ++blk_it;
           }
           umma_commit(&sm->kv_empty[st]);
           ++kv_it;
         }
         if (!ok) break;
-        umma_commit(&sm->o_full);
+        if (has) {
+          umma_commit(&sm->o_full[t]);
+          ++q_it;
+        }
       }
     }
-  } else {
-    // ------------------------------------------------------------ softmax
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const int row = warp * 32 + lane;
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax group t
+    const int t = warp >> 2;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + 256u * t;
+    const uint32_t tO = tS + 128u;
     const float sl2 = args.scale_log2;
     const int nh = args.num_heads;
-    uint32_t item_it = 0, blk_it = 0;
-    for (int it = blockIdx.x; it < args.n_items; it += gridDim.x, ++item_it) {
+    uint32_t blk_it = 0, q_it = 0, turn_it = 0;
+    // group 1 hands the first turn to group 0
+    if (t == 1) mbar_arrive(&sm->turn[0]);
+    for (int it = blockIdx.x; it < args.n_items; it += gridDim.x) {
       const FwdWork w = decode_fwd(args, it);
       const FwdSeg& sg = args.segs[w.seg];
       const int nkb = (sg.k_len + kBlockN - 1) / kBlockN;
+      const bool has = tile_present(sg, w, t);
       float m_run = -INFINITY;
       float l_run = 0.f;
       bool ok = true;
-      for (int j = 0; j < nkb; ++j, ++blk_it) {
+      for (int j = 0; j < nkb; ++j, ++turn_it) {
         // all lanes must agree before the warp-wide tcgen05.ld below
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(&sm->s_full, blk_it & 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_SOFTMAX))) {
+                        (!has || mbar_wait(&sm->s_full[t], blk_it & 1u, abort_flag, &g_fwd_err,
+                                           ERR_TIMEOUT_SOFTMAX)) &&
+                            mbar_wait(&sm->turn[t], turn_it & 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_SOFTMAX))) {
           ok = false;
           break;
+        }
+        if (!has) {
+          mbar_arrive(&sm->turn[t ^ 1]);
+          continue;
         }
         tc_fence_after();
         uint32_t s[4][32];
@@ -308,12 +359,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             const int c = 2 * hf + cc;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const uint64_t t = f2_fma(f2_pack(__uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1])),
+              const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1])),
                                         sl2x2, negm2);
-              float t0, t1;
-              f2_unpack(t, t0, t1);
-              const float a = fast_exp2(t0);
-              const float b = fast_exp2(t1);
+              float x0, x1;
+              f2_unpack(x, x0, x1);
+              const float a = fast_exp2(x0);
+              const float b = fast_exp2(x1);
               acc[i & 1] = f2_add(acc[i & 1], f2_pack(a, b));
               p[cc * 16 + i] = pack_bf16x2(a, b);
             }
@@ -322,6 +373,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         float ls0, ls1;
         f2_unpack(f2_add(acc[0], acc[1]), ls0, ls1);
+        // the exponentials are done: the other group may take its turn
+        mbar_arrive(&sm->turn[t ^ 1]);
         if (j > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
           for (int c = 0; c < HD / 32; ++c) {
@@ -336,16 +389,20 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&sm->p_full);
+        mbar_arrive(&sm->p_full[t]);
+        ++blk_it;
         l_run += ls0 + ls1;
       }
       if (!ok) break;
+      if (!has) continue;
       // ---------------------------------------------------------- epilogue
       if (!__all_sync(0xffffffffu,
-                      mbar_wait(&sm->o_full, item_it & 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_SOFTMAX)))
+                      mbar_wait(&sm->o_full[t], q_it & 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_SOFTMAX)))
         break;
+      ++q_it;
       tc_fence_after();
-      const int q_local = w.qb * kBlockM + row;
+      const int qb = 2 * w.qb + t;             // 128-row query block within the segment
+      const int q_local = qb * kBlockM + row;
       const bool row_ok = q_local < sg.q_len;
       const float inv_l = 1.f / l_run;
       const float lse_val = (m_run + log2f(l_run)) * kLn2;
@@ -392,15 +449,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (row_ok)
           args.lse_part[(static_cast<size_t>(sg.slot) * nh + w.h) * args.part_rows + sg.out_row0 + q_local] =
               lse_val;
-        // Fused merge: publish this partial; the CTA that completes the set
+        // Fused merge: publish this partial; the group that completes the set
         // of kv chunks of this (query block, head) merges them into o / lse.
         if (!args.fused_merge) continue;
         __threadfence();
-        named_bar_sync(1, 128);
+        named_bar_sync(1 + t, 128);
         if (row == 0)
-          sm->is_last = atomicAdd(args.counters + sg.counter0 + w.qb * nh + w.h, 1) == sg.n_kv - 1;
-        named_bar_sync(1, 128);
-        if (sm->is_last) {
+          sm->is_last[t] = atomicAdd(args.counters + sg.counter0 + qb * nh + w.h, 1) == sg.n_kv - 1;
+        named_bar_sync(1 + t, 128);
+        if (sm->is_last[t]) {
           __threadfence();
           if (row_ok) merge_tile_row<HD>(args, sg, w.h, q_local);
         }
@@ -414,7 +471,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp0) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int HD>

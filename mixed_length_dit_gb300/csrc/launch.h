@@ -12,12 +12,16 @@ namespace zl {
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 
+// Query rows per work item of the tensor-core forward: two 128-row tiles
+// that share every K/V tile.
+constexpr int kFwdRowsPerItem = 2 * kBlockM;
+
 // Work segments passed by value in one launch (kernel parameter space).
 constexpr int kMaxSegs = 640;
 
 // One segment of forward work: a whole sequence or one shard tile.  Its work
-// items are (head of [h0, h0 + nh), 128-row query block) pairs, numbered from
-// item0 with the query block fastest.
+// items are (head of [h0, h0 + nh), query block of rows_per_item rows) pairs,
+// numbered from item0 with the query block fastest.
 struct FwdSeg {
   int32_t q_row0;    // packed row of the segment's first query
   int32_t k_row0;    // packed row of the segment's first key
@@ -46,6 +50,7 @@ struct FwdArgs {
   float scale_log2;     // scale * log2(e)
   int32_t n_items;
   int32_t n_segs;
+  int32_t rows_per_item;  // query rows per work item: 256 (tensor cores, two tiles) or 128 (float32)
   FwdSeg segs[kMaxSegs];
 };
 static_assert(sizeof(FwdArgs) <= 32764, "forward arguments exceed the kernel parameter space");

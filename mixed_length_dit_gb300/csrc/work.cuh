@@ -1,6 +1,6 @@
 // Work-item decoding shared by the forward kernels: the host scheduler
 // numbers items segment by segment (head-major over the segment's head range,
-// 128-row query block fastest).
+// query block of a.rows_per_item rows fastest).
 #pragma once
 #include "launch.h"
 
@@ -19,7 +19,7 @@ __device__ __forceinline__ FwdWork decode_fwd(const FwdArgs& a, int it) {
     if (a.segs[mid].item0 <= it) lo = mid; else hi = mid - 1;
   }
   const FwdSeg& s = a.segs[lo];
-  const int nqb = (s.q_len + kBlockM - 1) / kBlockM;
+  const int nqb = (s.q_len + a.rows_per_item - 1) / a.rows_per_item;
   const int local = it - s.item0;
   return {lo, s.h0 + local / nqb, local % nqb};
 }

@@ -381,14 +381,15 @@ std::vector<Segment> schedule_fwd(const Plan& p, const int32_t* cu_q, const int3
 }
 
 // Fills args.segs with segments [first, last) and numbers their items.
-void fill_args(FwdArgs* args, const std::vector<Segment>& segs, size_t first, size_t last) {
+void fill_args(FwdArgs* args, const std::vector<Segment>& segs, size_t first, size_t last, int rows_per_item) {
   int64_t items = 0;
   args->n_segs = static_cast<int32_t>(last - first);
+  args->rows_per_item = rows_per_item;
   for (size_t i = first; i < last; ++i) {
     FwdSeg s = segs[i].seg;
     s.item0 = static_cast<int32_t>(items);
     args->segs[i - first] = s;
-    items += int64_t(s.nh) * ((s.q_len + kBlockM - 1) / kBlockM);
+    items += int64_t(s.nh) * ((s.q_len + rows_per_item - 1) / rows_per_item);
   }
   args->n_items = static_cast<int32_t>(items);
 }
@@ -531,10 +532,10 @@ zl_status zl_varlen_attn_fwd_ex(const void* q, const void* k, const void* v, con
   }
   for (size_t first = 0; first < segs.size(); first += kMaxSegs) {
     const size_t last = std::min(segs.size(), first + kMaxSegs);
-    fill_args(&args, segs, first, last);
+    fill_args(&args, segs, first, last, dtype == ZL_BF16 ? zl::kFwdRowsPerItem : kBlockM);
     if (args.n_items == 0) continue;
     if (dtype == ZL_BF16) {
-      const int grid = std::min(args.n_items, 2 * sms);
+      const int grid = std::min(args.n_items, sms);
       st = launch_counted("fwd_tc", s, [&] { return zl::launch_fwd_tc(head_dim, mq, mk, mv, args, grid, s); });
     } else {
       st = launch_counted("fwd_f32", s, [&] {

@@ -214,7 +214,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const int t = warp - kMmaWarp0;
       constexpr uint32_t idesc_qk = idesc_bf16(kBlockM, kBlockN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(kBlockM, HD, false, true);
-      const uint32_t q_addr = smem_u32(sm->q[t]);
+      // Operand descriptors: the start-address field holds (address >> 4), so
+      // the descriptor of a k-step is the tile's base descriptor plus the
+      // step's byte offset >> 4 (no carry: shared addresses stay below 256 KB).
+      // Building them this way keeps the issuing thread's per-MMA work short.
+      const uint64_t q_desc = sdesc_sw128(smem_u32(sm->q[t]), 16, 1024);
       const uint32_t tS = tmem + 256u * t;
       const uint32_t tO = tS + 128u;
       uint32_t kv_it = 0, q_it = 0, blk_it = 0;
@@ -238,12 +242,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           }
           tc_fence_after();
           if (has) {
-            const uint32_t k_addr = smem_u32(sm->kv[st]);
+            const uint64_t k_desc = sdesc_sw128(smem_u32(sm->kv[st]), 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < HD / 16; ++ks) {
-              const uint32_t off = (ks >> 2) * (kBlockM * 128) + (ks & 3) * 32;
-              umma_ss(tS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                      idesc_qk, ks > 0 ? 1u : 0u);
+              const uint64_t off16 = ((ks >> 2) * (kBlockM * 128) + (ks & 3) * 32) >> 4;
+              umma_ss(tS, q_desc + off16, k_desc + off16, idesc_qk, ks > 0 ? 1u : 0u);
             }
             umma_commit(&sm->s_full[t]);
             // Q_t is read by S MMAs only: after the item's last one the
@@ -262,11 +265,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           }
           tc_fence_after();
           if (has) {
-            const uint32_t v_addr = smem_u32(sm->kv[st]);
+            const uint64_t v_desc = sdesc_sw128(smem_u32(sm->kv[st]), kBlockN * 128, 1024);
 #pragma unroll
             for (int ks = 0; ks < kBlockN / 16; ++ks) {
-              umma_ts(tO, tS + ks * 8, sdesc_sw128(v_addr + ks * 2048, kBlockN * 128, 1024),
-                      idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+              umma_ts(tO, tS + ks * 8, v_desc + static_cast<uint64_t>(ks * (2048 >> 4)), idesc_pv,
+                      (j > 0 || ks > 0) ? 1u : 0u);
             }
             ++blk_it;
           }

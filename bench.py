@@ -1,7 +1,7 @@
 """Benchmark of the coalesced varlen attention hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 1..5] [--mode step|fwd]
+                    [--workload 1..8] [--mode step|fwd] [--seed S]
 
 One step = one pass of the whole path over one batch: the forward over whole
 sequences and shard tiles in one launch, the exact LSE merge of the tiles, the
@@ -215,6 +215,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=5)
+    ap.add_argument("--seed", type=int, default=0, help="input seed (rank r draws with seed + r)")
     ap.add_argument("--mode", choices=["step", "fwd"], default="step")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -244,7 +245,7 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     dev = torch.device("cuda", local_rank)
-    inp = synth.make_inputs(wl, seed=rank, device=dev)
+    inp = synth.make_inputs(wl, seed=args.seed + rank, device=dev)
     cu = wl.cu_seqlens()
     tiles = wl.tiles() or None
     H, D, T = wl.num_heads, wl.head_dim, wl.total_tokens
@@ -447,7 +448,7 @@ def main():
 def run_reference(args, wl, world):
     """The float64 CPU oracle, as it stands, on a bounded sample of the same
     workload: each step is the fwd+bwd of one head of one sequence."""
-    g = torch.Generator().manual_seed(0)
+    g = torch.Generator().manual_seed(args.seed)
     target = 4096
     lens = wl.seqlens
     s = min(range(len(lens)), key=lambda i: (abs(lens[i] - target), i))

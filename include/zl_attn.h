@@ -130,7 +130,7 @@ zl_status zl_varlen_attn_fwd_workspace_size(
  * workspace                    device, >= zl_varlen_attn_fwd_workspace_size
  *
  * Whole sequences and every tile run in one persistent launch whose work
- * items (sequence-or-tile x head of its range x 128-query block) are ordered
+ * items (sequence-or-tile x head of its range x query block) are ordered
  * longest first, ties in input order.  Tiles of key-split sequences write
  * float32 partials into the workspace, and a merge launch per such sequence
  * (zl_lse_merge's kernel) then combines each query row's partials into o and

@@ -337,7 +337,7 @@ def main():
     # host-to-device and device-to-host copies).
     e2e = None
     if not args.no_e2e:
-        k_e2e = max(2, min(args.steps, 6))
+        k_e2e = max(2, args.steps)
         names_in = ("q", "k", "v", "do")
         names_out = ("o", "dq", "dk", "dv") if step_bwd else ("o",)
         host_in = {n: inp[n].to("cpu").pin_memory() for n in names_in}

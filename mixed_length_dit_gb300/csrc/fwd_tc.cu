@@ -318,28 +318,43 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         tc_fence_after();
         uint32_t s[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, s[c]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) reg_fence(s[c]);
         const int valid = sg.k_len - j * kBlockN;
-        if (valid < kBlockN) {
+        float m_raw;
+        if (valid >= kBlockN) {
+          // full block: the reducing TMEM load returns each 32-column max
+          float r[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) r[c] = tmem_ld32_max(tS + lane_off + c * 32, s[c]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            reg_fence(s[c]);
+            reg_fence_f(r[c]);
+          }
+          m_raw = fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3]));
+        } else {
+          // last block of the segment: columns past its keys do not count
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, s[c]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) reg_fence(s[c]);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (c * 32 + i >= valid) s[c][i] = __float_as_uint(-INFINITY);
-        }
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          mx0 = fmax3(mx0, __uint_as_float(s[0][i]), __uint_as_float(s[0][i + 1]));
-          mx1 = fmax3(mx1, __uint_as_float(s[1][i]), __uint_as_float(s[1][i + 1]));
-          mx2 = fmax3(mx2, __uint_as_float(s[2][i]), __uint_as_float(s[2][i + 1]));
-          mx3 = fmax3(mx3, __uint_as_float(s[3][i]), __uint_as_float(s[3][i + 1]));
+          for (int i = 0; i < 32; i += 2) {
+            mx0 = fmax3(mx0, __uint_as_float(s[0][i]), __uint_as_float(s[0][i + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(s[1][i]), __uint_as_float(s[1][i + 1]));
+            mx2 = fmax3(mx2, __uint_as_float(s[2][i]), __uint_as_float(s[2][i + 1]));
+            mx3 = fmax3(mx3, __uint_as_float(s[3][i]), __uint_as_float(s[3][i + 1]));
+          }
+          m_raw = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
         }
-        const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const float m_blk = m_raw * sl2;
         const float m_new = fmaxf(m_run, m_blk);
         const bool need = m_new > m_run + kRescaleThreshold;
         float alpha = 1.f;

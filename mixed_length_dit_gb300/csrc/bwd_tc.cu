@@ -54,9 +54,9 @@ constexpr int kSgThreads = 256;
 constexpr int kDrainThreads = 128;
 constexpr int kDrainWarp0 = 8;
 constexpr int kProducerWarp = 12;
-constexpr int kMmaWarpA = 13;               // S^T, dV      (everything on S[b])
-constexpr int kMmaWarpB = 14;               // dP^T, dK     (everything on DP[b])
-constexpr int kMmaWarpC = 15;               // dQ^T         (into S[b] after dV)
+constexpr int kMmaWarpA = 13;               // S^T (into S[b]), dV
+constexpr int kMmaWarpB = 14;               // dP^T (into DP), dK
+constexpr int kMmaWarpC = 15;               // dQ^T (into DQ)
 constexpr int kQdStages = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -103,8 +103,8 @@ __device__ __forceinline__ void drain_delay(uint64_t ns) {
   }
 }
 
-// TMEM column (relative to S[b] / DP[b]) of the bf16 operand (P^T or dS^T) for
-// query k-step ks: queries 32h..32h+31 of the block live at [32h, 32h+16).
+// TMEM column (relative to S[b]) of the bf16 operand P^T for query k-step ks:
+// queries 32h..32h+31 of the block live at [32h, 32h+16).
 __device__ __forceinline__ uint32_t op_col(int ks) { return (ks >> 1) * 32 + (ks & 1) * 8; }
 
 // LSE*log2e (threads 0-63) or D (threads 64-127) of query row t of block i;

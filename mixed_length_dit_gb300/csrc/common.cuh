@@ -264,6 +264,33 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- cluster launch control
+// Work stealing across a grid of one CTA per work item: a running CTA asks the
+// hardware to cancel the launch of a CTA that has not started and takes over
+// its index.  The 16-byte answer lands in `resp` (16-byte aligned shared
+// memory) and completes 16 transaction bytes on `bar`.  After one answer
+// that cancelled nothing, the grid has no unstarted CTA left and no further
+// request may be made.
+__device__ __forceinline__ void clc_try_cancel(void* resp, uint64_t* bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+      :: "r"(smem_u32(resp)), "r"(smem_u32(bar)) : "memory");
+}
+
+// Reads an answer once its mbarrier phase has completed: the x index of the
+// cancelled CTA, or -1 if the request cancelled none.
+__device__ __forceinline__ int clc_cancelled_x(const void* resp) {
+  int x;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%1];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "mov.s32 %0, -1;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}"
+      : "=r"(x) : "r"(smem_u32(resp)) : "memory");
+  return x;
+}
+
 // Named barrier over `count` threads (id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");

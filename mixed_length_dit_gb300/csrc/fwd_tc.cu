@@ -5,12 +5,17 @@
 // sequence or one shard tile of a split sequence (Zellige, arXiv
 // 2608.01150v1, §IV-D: whole sequences packed into one block-diagonal call,
 // shards alongside them).  Items arrive ordered longest-first from the host
-// scheduler and are taken in a static stride by the CTAs, one CTA per SM.
+// scheduler.  The grid holds one CTA per item, of which one per SM is
+// resident; a resident CTA takes its own item first and then steals the
+// lowest unstarted one from the launch queue (cluster launch control), so an
+// SM that finishes early picks up the next item in longest-first order.
 //
 // The two query tiles of an item share every K_j / V_j tile that the producer
 // brings into shared memory.  Per CTA (352 threads):
 //   warp 8      TMA producer: the two Q tiles once per item, then K_j / V_j
 //               through a four-stage ring (128-byte swizzle, 64-column boxes).
+//               It also steals the next item and hands it to the other roles
+//               through a two-slot ring in shared memory.
 //   warps 9,10  MMA issuers, one thread each, one per query tile t:
 //               S_t = Q_t K_j^T (SS, M=128 N=128) into TMEM, then
 //               O_t += P_t V_j (TS: P read from TMEM, V from shared memory as
@@ -49,6 +54,7 @@ constexpr int kFwdThreads = 352;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp0 = 9;                 // tile 0; tile 1 is kMmaWarp0 + 1
 constexpr int kFwdStages = 4;
+constexpr int kItemReaders = 10;             // 2 issuer threads + 8 softmax warps
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;   // in log2 units: P <= 2^8
 constexpr float kLn2 = 0.6931471805599453f;
@@ -61,6 +67,10 @@ struct FwdSmem {
   uint64_t kv_full[kFwdStages], kv_empty[kFwdStages];
   uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t turn[2];                            // softmax group t may run its next block
+  uint64_t item_full[2], item_empty[2];        // ring of item indices, producer -> other roles
+  uint64_t steal_bar;                          // answer of a launch-cancel request landed
+  alignas(16) uint8_t steal_resp[16];
+  int item[2];                                 // item index, or -1: no further item
   uint32_t tmem_base;
   int abort_flag;
   int is_last[2];                              // group t completed a row block's partials
@@ -121,6 +131,22 @@ __device__ __forceinline__ bool tile_present(const FwdSeg& sg, const FwdWork& w,
   return (2 * w.qb + t) * kBlockM < sg.q_len;
 }
 
+// Takes the n-th item index of this CTA from the producer's ring: -1 once the
+// grid has no item left, -2 if the wait failed.  With `warp_wide` every lane
+// of the warp calls it and lane 0 releases the slot for the warp.
+template <int HD>
+__device__ __forceinline__ int take_item(FwdSmem<HD>* sm, uint32_t n, volatile int* abort_flag, uint32_t code,
+                                         bool warp_wide) {
+  const uint32_t s = n & 1u;
+  bool ok = mbar_wait(&sm->item_full[s], (n >> 1) & 1u, abort_flag, &g_fwd_err, code);
+  if (warp_wide) ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return -2;
+  const int it = *reinterpret_cast<volatile int*>(&sm->item[s]);
+  if (warp_wide) __syncwarp();
+  if (!warp_wide || (threadIdx.x & 31) == 0) mbar_arrive(&sm->item_empty[s]);
+  return it;
+}
+
 // Registers are granted per group of four warps, so 352 threads leave at
 // most 168 registers per thread.
 template <int HD>
@@ -147,6 +173,11 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_init(&sm->kv_full[s], 1);
       mbar_init(&sm->kv_empty[s], 2);          // both issuers are done with the stage
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm->item_full[s], 1);
+      mbar_init(&sm->item_empty[s], kItemReaders);
+    }
+    mbar_init(&sm->steal_bar, 1);
     sm->abort_flag = 0;
     fence_mbar_init();
   }
@@ -166,12 +197,17 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       tma_prefetch_map(&tmV);
       uint32_t kv_it = 0;
       uint32_t q_it[2] = {0u, 0u};
+      uint32_t steal_ph = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x) {
-        const FwdWork w = decode_fwd(args, it);
+      // the CTA's own item comes first
+      sm->item[0] = static_cast<int>(blockIdx.x);
+      mbar_arrive(&sm->item_full[0]);
+      for (uint32_t n = 1, it = blockIdx.x; ok; ++n) {
+        const FwdWork w = decode_fwd(args, static_cast<int>(it));
         const FwdSeg& sg = args.segs[w.seg];
         const int nkb = (sg.k_len + kBlockN - 1) / kBlockN;
         const int x0 = w.h * HD;
+        bool asked = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (!tile_present(sg, w, t)) continue;
           if (!mbar_wait(&sm->q_empty[t], (q_it[t] & 1u) ^ 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_PRODUCER)) {
@@ -186,6 +222,14 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tma_load_2d(sm->q[t] + c * kBlockM * 128, &tmQ, &sm->q_full[t], x0 + c * 64, q_row);
         }
         for (int j = 0; j < nkb && ok; ++j) {
+          if (j == nkb - 1) {
+            // the item's last K/V tiles are next: ask for the following item
+            // now, about two key blocks before the issuers need it
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&sm->steal_bar, 16);
+            clc_try_cancel(sm->steal_resp, &sm->steal_bar);
+            asked = true;
+          }
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
             const uint32_t st = kv_it % kFwdStages;
@@ -203,6 +247,27 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             ++kv_it;
           }
         }
+        if (!ok) break;
+        if (!asked) {                          // an item without keys
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(&sm->steal_bar, 16);
+          clc_try_cancel(sm->steal_resp, &sm->steal_bar);
+        }
+        if (!mbar_wait(&sm->steal_bar, steal_ph, abort_flag, &g_fwd_err, ERR_TIMEOUT_PRODUCER)) break;
+        steal_ph ^= 1u;
+        int next = clc_cancelled_x(sm->steal_resp);
+        if (next >= args.n_items) {            // not a CTA of this grid: stop here
+          atomicOr(&g_fwd_err, ERR_BAD_WORK);
+          next = -1;
+        }
+        // publish it once the readers of slot n & 1 have taken its previous index
+        if (!mbar_wait(&sm->item_empty[n & 1u], ((n >> 1) & 1u) ^ 1u, abort_flag, &g_fwd_err,
+                       ERR_TIMEOUT_PRODUCER))
+          break;
+        sm->item[n & 1u] = next;
+        mbar_arrive(&sm->item_full[n & 1u]);
+        if (next < 0) break;
+        it = static_cast<uint32_t>(next);
       }
     }
   } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
@@ -223,7 +288,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const uint32_t tO = tS + 128u;
       uint32_t kv_it = 0, q_it = 0, blk_it = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x) {
+      for (uint32_t n = 0; ok; ++n) {
+        const int it = take_item(sm, n, abort_flag, ERR_TIMEOUT_MMA, false);
+        if (it < 0) break;
         const FwdWork w = decode_fwd(args, it);
         const FwdSeg& sg = args.segs[w.seg];
         const int nkb = (sg.k_len + kBlockN - 1) / kBlockN;
@@ -295,7 +362,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     uint32_t blk_it = 0, q_it = 0, turn_it = 0;
     // group 1 hands the first turn to group 0
     if (t == 1) mbar_arrive(&sm->turn[0]);
-    for (int it = blockIdx.x; it < args.n_items; it += gridDim.x) {
+    for (uint32_t n = 0;; ++n) {
+      const int it = take_item(sm, n, abort_flag, ERR_TIMEOUT_SOFTMAX, true);
+      if (it < 0) break;
       const FwdWork w = decode_fwd(args, it);
       const FwdSeg& sg = args.segs[w.seg];
       const int nkb = (sg.k_len + kBlockN - 1) / kBlockN;

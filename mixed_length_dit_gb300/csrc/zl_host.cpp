@@ -535,7 +535,8 @@ zl_status zl_varlen_attn_fwd_ex(const void* q, const void* k, const void* v, con
     fill_args(&args, segs, first, last, dtype == ZL_BF16 ? zl::kFwdRowsPerItem : kBlockM);
     if (args.n_items == 0) continue;
     if (dtype == ZL_BF16) {
-      const int grid = std::min(args.n_items, sms);
+      // one CTA per item: the resident ones steal the rest in launch order
+      const int grid = args.n_items;
       st = launch_counted("fwd_tc", s, [&] { return zl::launch_fwd_tc(head_dim, mq, mk, mv, args, grid, s); });
     } else {
       st = launch_counted("fwd_f32", s, [&] {

@@ -216,8 +216,7 @@ extern "C" zl_status zl_varlen_attn_bwd_static(
     }
     args.n_segs = n;
     args.n_items = static_cast<int32_t>(items);
-    const int grid = static_cast<int>(std::min<int64_t>(items, sms));
-    if (zl::launch_bwd_tc(head_dim, mq, mk, mv, mdo, mdq, args, grid, s) != cudaSuccess) {
+    if (zl::launch_bwd_tc(head_dim, mq, mk, mv, mdo, mdq, args, s) != cudaSuccess) {
       cudaGetLastError();
       return ZL_ECUDA;
     }

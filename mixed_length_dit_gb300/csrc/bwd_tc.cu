@@ -40,6 +40,10 @@
 // TMEM lanes 32*(w%4).. and query columns 32*(w/4)..) and the dV/dK epilogue,
 // warps 8-11 dQ drain, warp 12 TMA producer (4-stage Q/dO ring), warps 13-15
 // MMA issuers.  Every wait is bounded.
+// The grid holds one CTA per item, ordered longest-first by the host; the
+// resident CTA of an SM takes its own item, then the producer steals the next
+// unstarted one from the launch queue (cluster launch control) and hands its
+// index to the other roles.
 #include "common.cuh"
 #include "launch.h"
 
@@ -58,6 +62,7 @@ constexpr int kMmaWarpA = 13;               // S^T (into S[b]), dV
 constexpr int kMmaWarpB = 14;               // dP^T (into DP), dK
 constexpr int kMmaWarpC = 15;               // dQ^T (into DQ)
 constexpr int kQdStages = 4;
+constexpr int kItemReaders = 15;             // issuers A, B, C + 4 drain warps + 8 softmax-grad warps
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -75,6 +80,7 @@ struct BwdSmem {
   uint64_t s_full[2], sg_done[2], ds_free[2];
   uint64_t dp_free, dq_full, dq_drained;
   uint64_t stage_full, dkdv_full, dkdv_drained;
+  ItemRing ring;                                  // work items, producer -> the other roles
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -149,6 +155,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(&sm->stage_full, kSgThreads);
     mbar_init(&sm->dkdv_full, 2);
     mbar_init(&sm->dkdv_drained, kSgThreads);
+    ring_init(&sm->ring, kItemReaders);
     sm->abort_flag = 0;
     fence_mbar_init();
   }
@@ -172,10 +179,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
       tma_prefetch_map(&tmDO);
-      uint32_t item_it = 0, qd_it = 0;
-      bool ok = true;
-      for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x, ++item_it) {
-        const BwdWork w = decode_bwd(args, it);
+      uint32_t item_it = 0, qd_it = 0, steal_ph = 0;
+      // the CTA's own item comes first
+      bool ok = ring_publish(&sm->ring, 0, static_cast<int>(blockIdx.x), abort_flag, &g_bwd_err,
+                             ERR_TIMEOUT_PRODUCER);
+      for (uint32_t n = 1, it = blockIdx.x; ok; ++n, ++item_it) {
+        const BwdWork w = decode_bwd(args, static_cast<int>(it));
         const BwdSeg& sg = args.segs[w.seg];
         const int nqb = (sg.q_len + kBQ - 1) / kBQ;
         const int start = w.kb % nqb;
@@ -190,10 +199,17 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           tma_load_2d(sm->k + c * kBlockN * 128, &tmK, &sm->kv_full, x0 + c * 64, sg.k_row0 + w.kb * kBlockN);
           tma_load_2d(sm->v + c * kBlockN * 128, &tmV, &sm->kv_full, x0 + c * 64, sg.k_row0 + w.kb * kBlockN);
         }
+        bool asked = false;
         for (int ii = 0; ii < nqb; ++ii, ++qd_it) {
           const int i = (start + ii) % nqb;
           const uint32_t st = qd_it % kQdStages;
           const uint32_t ph = (qd_it / kQdStages) & 1u;
+          if (ii == nqb - 1) {
+            // the item's last Q/dO block is next: ask for the following item
+            // now, a few query blocks before the other roles need it
+            ring_ask(&sm->ring);
+            asked = true;
+          }
           if (!mbar_wait(&sm->qd_empty[st], ph ^ 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_PRODUCER)) {
             ok = false;
             break;
@@ -206,6 +222,14 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         sg.q_row0 + i * kBQ);
           }
         }
+        if (!ok) break;
+        if (!asked) ring_ask(&sm->ring);       // a key block without queries
+        const int next = ring_answer(&sm->ring, steal_ph, args.n_items, abort_flag, &g_bwd_err,
+                                     ERR_TIMEOUT_PRODUCER);
+        if (next == -2 ||
+            !ring_publish(&sm->ring, n, next, abort_flag, &g_bwd_err, ERR_TIMEOUT_PRODUCER) || next < 0)
+          break;
+        it = static_cast<uint32_t>(next);
       }
     }
   } else if (warp == kMmaWarpA || warp == kMmaWarpB) {
@@ -242,7 +266,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         umma_commit(&sm->s_full[b]);
         return true;
       };
-      for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x, ++item_it) {
+      for (uint32_t n = 0; ok; ++n, ++item_it) {
+        const int it = ring_take(&sm->ring, n, abort_flag, &g_bwd_err, err, false);
+        if (it < 0) break;
         const BwdWork w = decode_bwd(args, it);
         const BwdSeg& sg = args.segs[w.seg];
         const uint32_t nqb = static_cast<uint32_t>((sg.q_len + kBQ - 1) / kBQ);
@@ -302,7 +328,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const uint32_t k_addr = smem_u32(sm->k);
       uint32_t item_it = 0, g = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x, ++item_it) {
+      for (uint32_t n = 0; ok; ++n, ++item_it) {
+        const int it = ring_take(&sm->ring, n, abort_flag, &g_bwd_err, ERR_TIMEOUT_MMA, false);
+        if (it < 0) break;
         const BwdWork w = decode_bwd(args, it);
         const BwdSeg& sg = args.segs[w.seg];
         const int nqb = (sg.q_len + kBQ - 1) / kBQ;
@@ -340,7 +368,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const bool active = dw * 32 < HD;
     uint32_t g = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x) {
+    for (uint32_t n = 0; ok; ++n) {
+      const int it = ring_take(&sm->ring, n, abort_flag, &g_bwd_err, ERR_TIMEOUT_OTHER, true);
+      if (it < 0) break;
       const BwdWork w = decode_bwd(args, it);
       const BwdSeg& sg = args.segs[w.seg];
       const int nqb = (sg.q_len + kBQ - 1) / kBQ;
@@ -403,7 +433,9 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const float sl2 = args.scale_log2;
     uint32_t item_it = 0, g = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < args.n_items && ok; it += gridDim.x, ++item_it) {
+    for (uint32_t n = 0; ok; ++n, ++item_it) {
+      const int it = ring_take(&sm->ring, n, abort_flag, &g_bwd_err, ERR_TIMEOUT_SOFTMAX, true);
+      if (it < 0) break;
       const BwdWork w = decode_bwd(args, it);
       const BwdSeg& sg = args.segs[w.seg];
       const int nqb = (sg.q_len + kBQ - 1) / kBQ;
@@ -522,13 +554,13 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
 template <int HD>
 cudaError_t launch_hd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                      const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& args, int grid,
+                      const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& args,
                       cudaStream_t stream) {
   const size_t smem = sizeof(BwdSmem<HD>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  bwd_tc_kernel<HD><<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, args);
+  bwd_tc_kernel<HD><<<args.n_items, kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, tdq, args);
   return cudaGetLastError();
 }
 
@@ -542,9 +574,9 @@ size_t bwd_tc_smem_bytes(int head_dim) {
 
 cudaError_t launch_bwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
-                          const BwdArgs& args, int grid, cudaStream_t stream) {
-  if (head_dim == 64) return launch_hd<64>(tq, tk, tv, tdo, tdq, args, grid, stream);
-  if (head_dim == 128) return launch_hd<128>(tq, tk, tv, tdo, tdq, args, grid, stream);
+                          const BwdArgs& args, cudaStream_t stream) {
+  if (head_dim == 64) return launch_hd<64>(tq, tk, tv, tdo, tdq, args, stream);
+  if (head_dim == 128) return launch_hd<128>(tq, tk, tv, tdo, tdq, args, stream);
   return cudaErrorInvalidValue;
 }
 

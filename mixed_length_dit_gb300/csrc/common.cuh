@@ -291,6 +291,76 @@ __device__ __forceinline__ int clc_cancelled_x(const void* resp) {
   return x;
 }
 
+// ---------------------------------------------------------------- item ring
+// A persistent CTA's work items, handed from its producer thread to the other
+// roles: slot n % 2 holds the CTA's n-th item index, or -1 once the grid has
+// no item left.  The first index is the CTA's own; each later one is stolen
+// from the launch queue (clc_try_cancel), so items are taken in launch order
+// by whichever SM asks first.
+struct ItemRing {
+  uint64_t full[2], empty[2];
+  uint64_t steal_bar;
+  alignas(16) uint8_t steal_resp[16];
+  int item[2];
+};
+
+// One thread, before the CTA-wide barrier that follows mbarrier setup.
+__device__ __forceinline__ void ring_init(ItemRing* r, uint32_t readers) {
+  for (int s = 0; s < 2; ++s) {
+    mbar_init(&r->full[s], 1);
+    mbar_init(&r->empty[s], readers);
+  }
+  mbar_init(&r->steal_bar, 1);
+}
+
+// Producer: requests the next item (its answer comes from ring_answer).
+__device__ __forceinline__ void ring_ask(ItemRing* r) {
+  fence_proxy_async_smem();                     // the last answer was read before it is overwritten
+  mbar_arrive_expect_tx(&r->steal_bar, 16);
+  clc_try_cancel(r->steal_resp, &r->steal_bar);
+}
+
+// Producer: the answer to the last request: the stolen item index, -1 if
+// none was left (or the index is not one of the n_items of this grid, which
+// also records ERR_BAD_WORK), -2 if the wait failed.
+__device__ __forceinline__ int ring_answer(ItemRing* r, uint32_t& phase, int n_items, volatile int* abort_flag,
+                                           uint32_t* err, uint32_t code) {
+  if (!mbar_wait(&r->steal_bar, phase, abort_flag, err, code)) return -2;
+  phase ^= 1u;
+  const int x = clc_cancelled_x(r->steal_resp);
+  if (x >= n_items) {
+    atomicOr(err, ERR_BAD_WORK);
+    return -1;
+  }
+  return x;
+}
+
+// Producer: publishes the n-th item once every reader has taken slot n % 2's
+// previous index.
+__device__ __forceinline__ bool ring_publish(ItemRing* r, uint32_t n, int item, volatile int* abort_flag,
+                                             uint32_t* err, uint32_t code) {
+  const uint32_t s = n & 1u;
+  if (!mbar_wait(&r->empty[s], ((n >> 1) & 1u) ^ 1u, abort_flag, err, code)) return false;
+  r->item[s] = item;
+  mbar_arrive(&r->full[s]);
+  return true;
+}
+
+// Reader: the n-th item index (-1: no item left, -2: the wait failed).  With
+// `warp_wide` every lane of the warp calls it and lane 0 counts the warp as
+// one reader.
+__device__ __forceinline__ int ring_take(ItemRing* r, uint32_t n, volatile int* abort_flag, uint32_t* err,
+                                         uint32_t code, bool warp_wide) {
+  const uint32_t s = n & 1u;
+  bool ok = mbar_wait(&r->full[s], (n >> 1) & 1u, abort_flag, err, code);
+  if (warp_wide) ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return -2;
+  const int it = *reinterpret_cast<volatile int*>(&r->item[s]);
+  if (warp_wide) __syncwarp();
+  if (!warp_wide || (threadIdx.x & 31) == 0) mbar_arrive(&r->empty[s]);
+  return it;
+}
+
 // Named barrier over `count` threads (id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");

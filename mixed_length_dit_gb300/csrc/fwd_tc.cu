@@ -67,10 +67,7 @@ struct FwdSmem {
   uint64_t kv_full[kFwdStages], kv_empty[kFwdStages];
   uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t turn[2];                            // softmax group t may run its next block
-  uint64_t item_full[2], item_empty[2];        // ring of item indices, producer -> other roles
-  uint64_t steal_bar;                          // answer of a launch-cancel request landed
-  alignas(16) uint8_t steal_resp[16];
-  int item[2];                                 // item index, or -1: no further item
+  ItemRing ring;                               // work items, producer -> the other roles
   uint32_t tmem_base;
   int abort_flag;
   int is_last[2];                              // group t completed a row block's partials
@@ -131,22 +128,6 @@ __device__ __forceinline__ bool tile_present(const FwdSeg& sg, const FwdWork& w,
   return (2 * w.qb + t) * kBlockM < sg.q_len;
 }
 
-// Takes the n-th item index of this CTA from the producer's ring: -1 once the
-// grid has no item left, -2 if the wait failed.  With `warp_wide` every lane
-// of the warp calls it and lane 0 releases the slot for the warp.
-template <int HD>
-__device__ __forceinline__ int take_item(FwdSmem<HD>* sm, uint32_t n, volatile int* abort_flag, uint32_t code,
-                                         bool warp_wide) {
-  const uint32_t s = n & 1u;
-  bool ok = mbar_wait(&sm->item_full[s], (n >> 1) & 1u, abort_flag, &g_fwd_err, code);
-  if (warp_wide) ok = __all_sync(0xffffffffu, ok);
-  if (!ok) return -2;
-  const int it = *reinterpret_cast<volatile int*>(&sm->item[s]);
-  if (warp_wide) __syncwarp();
-  if (!warp_wide || (threadIdx.x & 31) == 0) mbar_arrive(&sm->item_empty[s]);
-  return it;
-}
-
 // Registers are granted per group of four warps, so 352 threads leave at
 // most 168 registers per thread.
 template <int HD>
@@ -173,11 +154,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_init(&sm->kv_full[s], 1);
       mbar_init(&sm->kv_empty[s], 2);          // both issuers are done with the stage
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm->item_full[s], 1);
-      mbar_init(&sm->item_empty[s], kItemReaders);
-    }
-    mbar_init(&sm->steal_bar, 1);
+    ring_init(&sm->ring, kItemReaders);
     sm->abort_flag = 0;
     fence_mbar_init();
   }
@@ -198,10 +175,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       uint32_t kv_it = 0;
       uint32_t q_it[2] = {0u, 0u};
       uint32_t steal_ph = 0;
-      bool ok = true;
       // the CTA's own item comes first
-      sm->item[0] = static_cast<int>(blockIdx.x);
-      mbar_arrive(&sm->item_full[0]);
+      bool ok = ring_publish(&sm->ring, 0, static_cast<int>(blockIdx.x), abort_flag, &g_fwd_err,
+                             ERR_TIMEOUT_PRODUCER);
       for (uint32_t n = 1, it = blockIdx.x; ok; ++n) {
         const FwdWork w = decode_fwd(args, static_cast<int>(it));
         const FwdSeg& sg = args.segs[w.seg];
@@ -225,9 +201,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           if (j == nkb - 1) {
             // the item's last K/V tiles are next: ask for the following item
             // now, about two key blocks before the issuers need it
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&sm->steal_bar, 16);
-            clc_try_cancel(sm->steal_resp, &sm->steal_bar);
+            ring_ask(&sm->ring);
             asked = true;
           }
 #pragma unroll
@@ -248,25 +222,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           }
         }
         if (!ok) break;
-        if (!asked) {                          // an item without keys
-          fence_proxy_async_smem();
-          mbar_arrive_expect_tx(&sm->steal_bar, 16);
-          clc_try_cancel(sm->steal_resp, &sm->steal_bar);
-        }
-        if (!mbar_wait(&sm->steal_bar, steal_ph, abort_flag, &g_fwd_err, ERR_TIMEOUT_PRODUCER)) break;
-        steal_ph ^= 1u;
-        int next = clc_cancelled_x(sm->steal_resp);
-        if (next >= args.n_items) {            // not a CTA of this grid: stop here
-          atomicOr(&g_fwd_err, ERR_BAD_WORK);
-          next = -1;
-        }
-        // publish it once the readers of slot n & 1 have taken its previous index
-        if (!mbar_wait(&sm->item_empty[n & 1u], ((n >> 1) & 1u) ^ 1u, abort_flag, &g_fwd_err,
-                       ERR_TIMEOUT_PRODUCER))
+        if (!asked) ring_ask(&sm->ring);       // an item without keys
+        const int next = ring_answer(&sm->ring, steal_ph, args.n_items, abort_flag, &g_fwd_err,
+                                     ERR_TIMEOUT_PRODUCER);
+        if (next == -2 ||
+            !ring_publish(&sm->ring, n, next, abort_flag, &g_fwd_err, ERR_TIMEOUT_PRODUCER) || next < 0)
           break;
-        sm->item[n & 1u] = next;
-        mbar_arrive(&sm->item_full[n & 1u]);
-        if (next < 0) break;
         it = static_cast<uint32_t>(next);
       }
     }
@@ -289,7 +250,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       uint32_t kv_it = 0, q_it = 0, blk_it = 0;
       bool ok = true;
       for (uint32_t n = 0; ok; ++n) {
-        const int it = take_item(sm, n, abort_flag, ERR_TIMEOUT_MMA, false);
+        const int it = ring_take(&sm->ring, n, abort_flag, &g_fwd_err, ERR_TIMEOUT_MMA, false);
         if (it < 0) break;
         const FwdWork w = decode_fwd(args, it);
         const FwdSeg& sg = args.segs[w.seg];
@@ -363,7 +324,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // group 1 hands the first turn to group 0
     if (t == 1) mbar_arrive(&sm->turn[0]);
     for (uint32_t n = 0;; ++n) {
-      const int it = take_item(sm, n, abort_flag, ERR_TIMEOUT_SOFTMAX, true);
+      const int it = ring_take(&sm->ring, n, abort_flag, &g_fwd_err, ERR_TIMEOUT_SOFTMAX, true);
       if (it < 0) break;
       const FwdWork w = decode_fwd(args, it);
       const FwdSeg& sg = args.segs[w.seg];
@@ -563,12 +524,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
 template <int HD>
 cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                      const FwdArgs& args, int grid, cudaStream_t stream) {
+                      const FwdArgs& args, cudaStream_t stream) {
   const size_t smem = sizeof(FwdSmem<HD>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  fwd_tc_kernel<HD><<<grid, kFwdThreads, smem, stream>>>(tq, tk, tv, args);
+  fwd_tc_kernel<HD><<<args.n_items, kFwdThreads, smem, stream>>>(tq, tk, tv, args);
   return cudaGetLastError();
 }
 
@@ -579,10 +540,9 @@ size_t fwd_tc_smem_bytes(int head_dim) {
 }
 
 cudaError_t launch_fwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const FwdArgs& args, int grid,
-                          cudaStream_t stream) {
-  if (head_dim == 64) return launch_tc<64>(tq, tk, tv, args, grid, stream);
-  if (head_dim == 128) return launch_tc<128>(tq, tk, tv, args, grid, stream);
+                          const CUtensorMap& tv, const FwdArgs& args, cudaStream_t stream) {
+  if (head_dim == 64) return launch_tc<64>(tq, tk, tv, args, stream);
+  if (head_dim == 128) return launch_tc<128>(tq, tk, tv, args, stream);
   return cudaErrorInvalidValue;
 }
 

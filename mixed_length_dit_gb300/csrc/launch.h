@@ -95,9 +95,10 @@ struct BwdArgs {
 
 // ---------------------------------------------------------------- launchers
 // Each returns the CUDA error of the launch (cudaSuccess when enqueued).
+// The tensor-core kernels are launched with one CTA per work item
+// (args.n_items): the CTAs resident at a time steal the unstarted ones.
 cudaError_t launch_fwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const FwdArgs& args, int grid,
-                          cudaStream_t stream);
+                          const CUtensorMap& tv, const FwdArgs& args, cudaStream_t stream);
 cudaError_t launch_fwd_f32(int head_dim, const float* q, const float* k, const float* v,
                            const FwdArgs& args, cudaStream_t stream);
 cudaError_t launch_merge(int head_dim, const MergeArgs& args, int num_sms, cudaStream_t stream);
@@ -113,7 +114,7 @@ int bwd_query_block();
 // into it with TMA).  args.dq_acc must be zeroed before the launch.
 cudaError_t launch_bwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
-                          const BwdArgs& args, int grid, cudaStream_t stream);
+                          const BwdArgs& args, cudaStream_t stream);
 cudaError_t launch_dq_convert(int head_dim, const float* dq_acc, void* dq, int64_t tq,
                               int32_t num_heads, float scale, int num_sms, cudaStream_t stream);
 

@@ -535,9 +535,7 @@ zl_status zl_varlen_attn_fwd_ex(const void* q, const void* k, const void* v, con
     fill_args(&args, segs, first, last, dtype == ZL_BF16 ? zl::kFwdRowsPerItem : kBlockM);
     if (args.n_items == 0) continue;
     if (dtype == ZL_BF16) {
-      // one CTA per item: the resident ones steal the rest in launch order
-      const int grid = args.n_items;
-      st = launch_counted("fwd_tc", s, [&] { return zl::launch_fwd_tc(head_dim, mq, mk, mv, args, grid, s); });
+      st = launch_counted("fwd_tc", s, [&] { return zl::launch_fwd_tc(head_dim, mq, mk, mv, args, s); });
     } else {
       st = launch_counted("fwd_f32", s, [&] {
         return zl::launch_fwd_f32(head_dim, static_cast<const float*>(q), static_cast<const float*>(k),
@@ -671,8 +669,7 @@ zl_status zl_varlen_attn_bwd(const void* q, const void* k, const void* v, const 
     }
     args.n_items = static_cast<int32_t>(items);
     if (items == 0) continue;
-    const int grid = static_cast<int>(std::min<int64_t>(items, sms));
-    st = launch_counted("bwd_tc", s, [&] { return zl::launch_bwd_tc(head_dim, mq, mk, mv, mdo, mdq, args, grid, s); });
+    st = launch_counted("bwd_tc", s, [&] { return zl::launch_bwd_tc(head_dim, mq, mk, mv, mdo, mdq, args, s); });
     if (st != ZL_OK) return st;
   }
   return launch_counted("dq_convert", s, [&] {

@@ -168,11 +168,17 @@ def fwd_flops(wl) -> float:
     return 4.0 * wl.head_dim * wl.num_heads * wl.pair_count()
 
 
-def merge_bytes(wl, launch_rows) -> float:
-    """Algorithmic bytes of one merge launch over `launch_rows` query rows."""
-    nparts = max(b for _, b in wl.splits.values())
+def merge_bytes(wl) -> float:
+    """Algorithmic bytes the merge moves per step: every sequence split over
+    keys (n_kv > 1; splits are (n_q, n_kv[, n_h])) reads its n_kv float32
+    partial rows and LSEs and writes its bf16 O rows and LSEs."""
     h, d = wl.num_heads, wl.head_dim
-    return launch_rows * h * (nparts * (4 * d + 4) + (2 * d + 4))
+    total = 0.0
+    for s, sp in wl.splits.items():
+        n_kv = sp[1]
+        if n_kv > 1:
+            total += wl.seqlens[s] * h * (n_kv * (4 * d + 4) + (2 * d + 4))
+    return total
 
 
 # ----------------------------------------------------------------- CPU oracle
@@ -307,10 +313,9 @@ def main():
                     "frac": round(ach / sustained, 4), "traffic": traffic,
                     "kernel": dom, "peak_kind": f"bf16 sustained ({peak_kind})",
                     "flops_per_launch": per_launch, "avg_launch_ms": round(avg_ms, 4)}
-        else:
+        elif dom == "lse_merge":
             hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-            rows = sum(wl.seqlens[s] for s in wl.splits)
-            per_launch = merge_bytes(wl, rows) * args.steps / max(1, n_l)
+            per_launch = merge_bytes(wl) * args.steps / max(1, n_l)
             ach = per_launch / (avg_ms * 1e-3) / 1e9
             roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                     "frac": round(ach / hbm, 4), "traffic": traffic, "kernel": dom}
@@ -323,7 +328,7 @@ def main():
         phases["bwd_tflops"] = round(2.5 * flops_fwd / (bwd_ms * 1e-3) / 1e12, 1)
     if "lse_merge" in prof and wl.splits:
         n_l, tot = prof["lse_merge"]
-        per_launch = merge_bytes(wl, sum(wl.seqlens[s] for s in wl.splits)) * args.steps / n_l
+        per_launch = merge_bytes(wl) * args.steps / n_l
         gbs = per_launch / (tot / n_l * 1e-3) / 1e9
         hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
         phases["merge"] = {"gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),

@@ -70,3 +70,17 @@ def test_reference_arm_prints_the_contract_line():
     assert d["value"] > 0 and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_merge_bytes_count_key_split_sequences_only():
+    """The merge reads n_kv float32 partials (O row + LSE) per row and head and
+    writes the bf16 row and its LSE, for sequences split over keys only:
+    tiles of query or head splits write their rows directly."""
+    import synth
+    wl = synth.config(8)                      # splits (1,1,4), (2,2,2), (2,1,5)
+    h, d = wl.num_heads, wl.head_dim
+    row = 2 * (4 * d + 4) + (2 * d + 4)
+    assert bench.merge_bytes(wl) == wl.seqlens[1] * h * row
+    wl5 = synth.config(5)                     # one sequence as 2 x 2 tiles
+    assert bench.merge_bytes(wl5) == wl5.seqlens[0] * wl5.num_heads * row
+    assert bench.merge_bytes(synth.config(2)) == 0

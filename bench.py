@@ -93,7 +93,8 @@ def workload_desc(wl) -> str:
     parts = []
     for n, c in sorted(counts.items(), key=lambda x: -x[0]):
         parts.append(f"{c}x{n}")
-    split = ", ".join(f"seq {s} ({wl.seqlens[s]} tokens) as {a}x{b} tiles" for s, (a, b) in wl.splits.items())
+    split = ", ".join(f"seq {s} ({wl.seqlens[s]} tokens) as {'x'.join(str(c) for c in sp)} tiles"
+                      for s, sp in wl.splits.items())
     return (f"{wl.name}: " + " + ".join(parts) + f" tokens; H={wl.num_heads}, d={wl.head_dim}"
             + (f"; {split}" if split else ""))
 

@@ -84,3 +84,16 @@ def test_merge_bytes_count_key_split_sequences_only():
     wl5 = synth.config(5)                     # one sequence as 2 x 2 tiles
     assert bench.merge_bytes(wl5) == wl5.seqlens[0] * wl5.num_heads * row
     assert bench.merge_bytes(synth.config(2)) == 0
+
+
+def test_workload_descriptions_cover_every_workload():
+    """Every workload bench.py can time describes itself (splits of two or
+    three chunk counts) and prices its merge without error."""
+    import synth
+    for n in range(1, 9):
+        wl = synth.config(n)
+        desc = bench.workload_desc(wl)
+        assert wl.name in desc
+        for s, sp in wl.splits.items():
+            assert f"as {'x'.join(str(c) for c in sp)} tiles" in desc
+        assert bench.merge_bytes(wl) >= 0

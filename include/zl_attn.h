@@ -131,7 +131,9 @@ zl_status zl_varlen_attn_fwd_workspace_size(
  *
  * Whole sequences and every tile run in one persistent launch whose work
  * items (sequence-or-tile x head of its range x query block) are ordered
- * longest first, ties in input order.  Tiles of key-split sequences write
+ * longest first, ties in input order; each SM takes the next item of that
+ * order when it is ready for one, so the launch balances itself.  It shares
+ * the GPU safely with concurrent launches on other streams.  Tiles of key-split sequences write
  * float32 partials into the workspace, and a merge launch per such sequence
  * (zl_lse_merge's kernel) then combines each query row's partials into o and
  * lse exactly; tiles of sequences split only by queries and heads write o and

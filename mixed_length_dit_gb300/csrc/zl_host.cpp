@@ -8,9 +8,11 @@
 // (§IV-C, Eq. 8 and Alg. 1) takes sequences in decreasing price.  On one GPU
 // the same largest-first idea becomes: every segment (whole sequence or tile)
 // is costed by the keys each of its 128-row query blocks must visit, segments
-// are stably sorted by decreasing cost (ties keep input order), and the
-// persistent grid takes work items in that order so the long video blocks
-// start first and the cheap image blocks fill the tail.
+// are stably sorted by decreasing cost (ties keep input order) and numbered
+// into work items in that order.  The kernels launch one CTA per item; the
+// resident CTA of each SM steals the next unstarted item when it needs one,
+// so the long video blocks start first and the cheap image blocks fill the
+// tail on whichever SMs come free.
 #include <algorithm>
 #include <atomic>
 #include <cmath>

@@ -301,3 +301,46 @@ def test_fused_merge_matches_separate_merge(n, hd):
     assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
     assert (l1 - l2).abs().max().item() <= 1e-5
     _full_check(inp["q"], inp["k"], inp["v"], cu, cu, o2, l2, TOL_O_BF16, TOL_LSE) if n == 1 else None
+
+
+def test_concurrent_launches_on_two_streams_bitwise():
+    """Two forward launches in flight at once on different streams: their CTAs
+    share the SMs, and each launch takes work only from its own queue, so
+    both give bit-identical results to the same launches run one after the
+    other (every work item done exactly once)."""
+    wa = synth.config(2)                                     # 28 sequences, 2,688 items
+    wb = synth.Workload("two_streams_b", [20000, 3000, 500, 1024, 1024], 8, 128, splits={0: (2, 2)})
+
+    def prep(wl, seed):
+        inp = synth.make_inputs(wl, seed=seed, device="cuda", with_grad_out=False)
+        cu = wl.cu_seqlens()
+        tiles = wl.tiles() or None
+        ws = zl.alloc_workspace(zl.fwd_workspace_bytes(cu, cu, wl.num_heads, wl.head_dim, tiles), "cuda")
+        o = torch.empty_like(inp["q"])
+        lse = torch.empty((wl.num_heads, wl.total_tokens), device="cuda")
+        return inp, cu, tiles, ws, o, lse
+
+    a, b = prep(wa, 3), prep(wb, 4)
+
+    def launch(x, stream):
+        inp, cu, tiles, ws, o, lse = x
+        zl.varlen_attn_fwd(inp["q"], inp["k"], inp["v"], cu, cu, tiles=tiles, out=o, lse=lse,
+                           workspace=ws, stream=stream)
+
+    launch(a, None)
+    launch(b, None)
+    torch.cuda.synchronize()
+    ref = [(x[4].clone(), x[5].clone()) for x in (a, b)]
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        for x in (a, b):
+            x[4].zero_()
+            x[5].zero_()
+        torch.cuda.synchronize()
+        launch(a, s1)
+        launch(b, s2)
+        torch.cuda.synchronize()
+        for x, (o_ref, l_ref) in zip((a, b), ref):
+            assert torch.equal(x[4], o_ref)
+            assert torch.equal(x[5], l_ref)
+    zl.sync_check()

@@ -169,16 +169,18 @@ def fwd_flops(wl) -> float:
     return 4.0 * wl.head_dim * wl.num_heads * wl.pair_count()
 
 
-def merge_bytes(wl) -> float:
+def merge_bytes(wl, bf16_partials: bool = False) -> float:
     """Algorithmic bytes the merge moves per step: every sequence split over
-    keys (n_kv > 1; splits are (n_q, n_kv[, n_h])) reads its n_kv float32
-    partial rows and LSEs and writes its bf16 O rows and LSEs."""
+    keys (n_kv > 1; splits are (n_q, n_kv[, n_h])) reads its n_kv partial rows
+    (float32, or bf16 with bf16_partials) and float32 LSEs and writes its bf16
+    O rows and LSEs."""
     h, d = wl.num_heads, wl.head_dim
+    part = (2 if bf16_partials else 4) * d + 4
     total = 0.0
     for s, sp in wl.splits.items():
         n_kv = sp[1]
         if n_kv > 1:
-            total += wl.seqlens[s] * h * (n_kv * (4 * d + 4) + (2 * d + 4))
+            total += wl.seqlens[s] * h * (n_kv * part + (2 * d + 4))
     return total
 
 
@@ -226,6 +228,8 @@ def main():
     ap.add_argument("--mode", choices=["step", "fwd"], default="step")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bf16-partials", action="store_true",
+                    help="keep the partial O rows of key-split sequences in bf16")
     ap.add_argument("--oracle-tokens", type=int, default=4096,
                     help="length of the sequence whose heads the CPU oracle times")
     ap.add_argument("--oracle-heads", type=int, default=16,
@@ -264,7 +268,8 @@ def main():
     step_bwd = args.mode == "step"
 
     def step(q, k, v, do):
-        zl.varlen_attn_fwd(q, k, v, cu, cu, tiles=tiles, out=o, lse=lse, workspace=fws)
+        zl.varlen_attn_fwd(q, k, v, cu, cu, tiles=tiles, out=o, lse=lse, workspace=fws,
+                           bf16_partials=args.bf16_partials)
         if step_bwd:
             zl.varlen_attn_bwd(q, k, v, o, lse, do, cu, cu, tiles=tiles, dq=dq, dk=dk, dv=dv, workspace=bws)
 
@@ -316,7 +321,7 @@ def main():
                     "flops_per_launch": per_launch, "avg_launch_ms": round(avg_ms, 4)}
         elif dom == "lse_merge":
             hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-            per_launch = merge_bytes(wl) * args.steps / max(1, n_l)
+            per_launch = merge_bytes(wl, args.bf16_partials) * args.steps / max(1, n_l)
             ach = per_launch / (avg_ms * 1e-3) / 1e9
             roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                     "frac": round(ach / hbm, 4), "traffic": traffic, "kernel": dom}
@@ -329,7 +334,7 @@ def main():
         phases["bwd_tflops"] = round(2.5 * flops_fwd / (bwd_ms * 1e-3) / 1e12, 1)
     if "lse_merge" in prof and wl.splits:
         n_l, tot = prof["lse_merge"]
-        per_launch = merge_bytes(wl) * args.steps / n_l
+        per_launch = merge_bytes(wl, args.bf16_partials) * args.steps / n_l
         gbs = per_launch / (tot / n_l * 1e-3) / 1e9
         hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
         phases["merge"] = {"gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
@@ -369,7 +374,7 @@ def main():
             comp.wait_event(ev["h2d"][sl])
             comp.wait_event(ev["d2h"][sl])                # step i-2's results have left this slot
             zl.varlen_attn_fwd(din["q"], din["k"], din["v"], cu, cu, tiles=tiles, out=dout["o"],
-                               lse=lse2[sl], workspace=fws)
+                               lse=lse2[sl], workspace=fws, bf16_partials=args.bf16_partials)
             if step_bwd:
                 zl.varlen_attn_bwd(din["q"], din["k"], din["v"], dout["o"], lse2[sl], din["do"], cu, cu,
                                    tiles=tiles, dq=dout["dq"], dk=dout["dk"], dv=dout["dv"], workspace=bws)
@@ -436,7 +441,8 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "no flush: every input tensor (>= %.2f GB) is larger than the 129 MB L2"
                          % (wl.total_tokens * H * D * 2 / 1e9),
-                   "flops_per_step": flops_step},
+                   "flops_per_step": flops_step,
+                   "partials": "bf16" if args.bf16_partials else "float32"},
         "pct_of_peak": round(100 * value / world / bf16_peak, 2),
         "peak_tflops": bf16_peak,
         "phases": phases,

@@ -156,7 +156,16 @@ enum {
    * zl_lse_merge; no waiting).  Saves the merge launch; measured slower than
    * the separate merge on the long-video batches, because the merging CTA's
    * tensor pipeline idles meanwhile.  bf16 only (ignored for ZL_FP32). */
-  ZL_FWD_FUSED_MERGE = 1
+  ZL_FWD_FUSED_MERGE = 1,
+  /* Tiles of key-split sequences write their partial O rows in bf16 instead
+   * of float32 (partial LSEs stay float32), which halves the bytes the
+   * partials move through HBM, and the merge (separate or fused) reads them
+   * back in bf16 and accumulates in float32.  Each partial row is rounded to
+   * bf16 once before the merge: an added error of at most 2^-9 of each
+   * partial's magnitude, inside the bf16 output's own rounding budget.  The
+   * workspace is the same (its float32 size is an upper bound).  bf16 only
+   * (ignored for ZL_FP32). */
+  ZL_FWD_BF16_PARTIALS = 2
 };
 
 /*
@@ -194,6 +203,18 @@ zl_status zl_varlen_attn_fwd_ex(
  */
 zl_status zl_lse_merge(
     const float* o_partial, const float* lse_partial, int32_t n_parts,
+    int64_t rows, int32_t num_heads, int32_t head_dim, int64_t part_stride_rows,
+    void* o, int32_t out_dtype, float* lse, int64_t lse_head_stride, void* stream);
+
+/*
+ * zl_lse_merge with the partial O rows in part_dtype: ZL_FP32 (exactly
+ * zl_lse_merge) or ZL_BF16 (the same layout in bf16 elements, as written by
+ * the forward under ZL_FWD_BF16_PARTIALS).  lse_partial stays float32 and
+ * the accumulation is float32 either way.  Other part_dtype values give
+ * ZL_EUNSUPPORTED; the other arguments and errors are zl_lse_merge's.
+ */
+zl_status zl_lse_merge_ex(
+    const void* o_partial, int32_t part_dtype, const float* lse_partial, int32_t n_parts,
     int64_t rows, int32_t num_heads, int32_t head_dim, int64_t part_stride_rows,
     void* o, int32_t out_dtype, float* lse, int64_t lse_head_stride, void* stream);
 

@@ -29,10 +29,11 @@ EXPORTS = (
     "zl_status_string", "zl_version", "zl_varlen_attn_fwd_workspace_size", "zl_varlen_attn_fwd",
     "zl_lse_merge", "zl_varlen_attn_bwd_workspace_size", "zl_varlen_attn_bwd", "zl_sync_check",
     "zl_launch_count", "zl_profile_begin", "zl_profile_end", "zl_varlen_attn_bwd_static",
-    "zl_varlen_attn_fwd_ex",
+    "zl_varlen_attn_fwd_ex", "zl_lse_merge_ex",
 )
 
 ZL_FWD_FUSED_MERGE = 1
+ZL_FWD_BF16_PARTIALS = 2
 
 
 class Tile(ctypes.Structure):
@@ -87,6 +88,8 @@ def load() -> ctypes.CDLL:
                                           tilep, c_i32, vp, vp, vp, c_sz, vp, ctypes.c_uint32]
     lib.zl_lse_merge.restype = c_i32
     lib.zl_lse_merge.argtypes = [vp, vp, c_i32, c_i64, c_i32, c_i32, c_i64, vp, c_i32, vp, c_i64, vp]
+    lib.zl_lse_merge_ex.restype = c_i32
+    lib.zl_lse_merge_ex.argtypes = [vp, c_i32, vp, c_i32, c_i64, c_i32, c_i32, c_i64, vp, c_i32, vp, c_i64, vp]
     lib.zl_varlen_attn_bwd_workspace_size.restype = c_i32
     lib.zl_varlen_attn_bwd_workspace_size.argtypes = [i32p, i32p, c_i32, c_i32, c_i32, szp]
     lib.zl_varlen_attn_bwd.restype = c_i32

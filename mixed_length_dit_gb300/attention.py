@@ -68,10 +68,12 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor | None:
 
 
 def varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k=None, tiles=None, softmax_scale=None,
-                    out=None, lse=None, workspace=None, stream=None, fused_merge=False):
+                    out=None, lse=None, workspace=None, stream=None, fused_merge=False,
+                    bf16_partials=False):
     """Coalesced block-diagonal attention forward.  Returns (o, lse).
     fused_merge merges tile partials inside the forward launch
-    (ZL_FWD_FUSED_MERGE)."""
+    (ZL_FWD_FUSED_MERGE); bf16_partials keeps the partial O rows of key-split
+    sequences in bf16 (ZL_FWD_BF16_PARTIALS)."""
     lib = _lib.load()
     if cu_seqlens_k is None:
         cu_seqlens_k = cu_seqlens_q
@@ -91,7 +93,7 @@ def varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k=None, tiles=None, softma
         raise ValueError("cu_seqlens_q and cu_seqlens_k differ in length")
     ta, nt = _lib.tile_array(tiles)
     ws_bytes = workspace.numel() if workspace is not None else 0
-    flags = _lib.ZL_FWD_FUSED_MERGE if fused_merge else 0
+    flags = (_lib.ZL_FWD_FUSED_MERGE if fused_merge else 0) | (_lib.ZL_FWD_BF16_PARTIALS if bf16_partials else 0)
     st = lib.zl_varlen_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), cq, ck, nq - 1, nh, hd, _dtype_code(q),
                                    scale, ta, nt, _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                    _stream_handle(stream), flags)
@@ -127,8 +129,8 @@ def varlen_attn_bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k=None, tile
 
 def lse_merge(o_partial, lse_partial, rows=None, out_dtype=torch.bfloat16, out=None, lse=None,
               lse_head_stride=None, stream=None):
-    """Exact merge of partials o_partial [P, R, H, d] / lse_partial [P, H, R]
-    (float32) into (o [rows, H, d], lse [H, rows])."""
+    """Exact merge of partials o_partial [P, R, H, d] (float32 or bf16) /
+    lse_partial [P, H, R] (float32) into (o [rows, H, d], lse [H, rows])."""
     lib = _lib.load()
     _check_tensor(o_partial, "o_partial")
     _check_tensor(lse_partial, "lse_partial")
@@ -140,10 +142,13 @@ def lse_merge(o_partial, lse_partial, rows=None, out_dtype=torch.bfloat16, out=N
         lse = torch.empty((nh, rows), dtype=torch.float32, device=o_partial.device)
         lse_head_stride = rows
     code = _lib.ZL_BF16 if out.dtype == torch.bfloat16 else _lib.ZL_FP32
-    st = lib.zl_lse_merge(_ptr(o_partial), _ptr(lse_partial), n_parts, rows, nh, hd, part_rows,
-                          _ptr(out), code, _ptr(lse), int(lse_head_stride or rows),
-                          _stream_handle(stream))
-    _lib.check(st, "zl_lse_merge")
+    part = _lib.ZL_BF16 if o_partial.dtype == torch.bfloat16 else _lib.ZL_FP32
+    if o_partial.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("o_partial must be float32 or bf16")
+    st = lib.zl_lse_merge_ex(_ptr(o_partial), part, _ptr(lse_partial), n_parts, rows, nh, hd, part_rows,
+                             _ptr(out), code, _ptr(lse), int(lse_head_stride or rows),
+                             _stream_handle(stream))
+    _lib.check(st, "zl_lse_merge_ex")
     return out, lse
 
 

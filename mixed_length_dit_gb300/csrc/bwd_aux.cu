@@ -16,10 +16,6 @@ namespace {
 
 constexpr int kAuxThreads = 256;
 
-__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {
-  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
-}
-
 template <int HD>
 __global__ void __launch_bounds__(kAuxThreads)
 bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,

@@ -374,6 +374,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Packed bf16x2 -> two floats (exact: a bf16 is the top half of a float32).
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
 // Two floats -> packed bf16x2 (round to nearest even); `lo` in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

@@ -95,15 +95,30 @@ __device__ __forceinline__ void merge_tile_row(const FwdArgs& a, const FwdSeg& s
     for (int e = 0; e < 32; ++e) acc[e] = 0.f;
     for (int j = 0; j < sg.n_kv; ++j) {
       const float wj = expf(__ldcg(a.lse_part + (static_cast<size_t>(j) * nh + h) * a.part_rows + prow) - m) * inv;
-      const float4* src = reinterpret_cast<const float4*>(
-          a.o_part + ((static_cast<size_t>(j) * a.part_rows + prow) * nh + h) * HD + c * 32);
+      const size_t off = ((static_cast<size_t>(j) * a.part_rows + prow) * nh + h) * HD + c * 32;
+      if (a.part_bf16) {
+        const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.o_part) + off);
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const float4 x = __ldcg(src + v);
-        acc[4 * v + 0] = fmaf(wj, x.x, acc[4 * v + 0]);
-        acc[4 * v + 1] = fmaf(wj, x.y, acc[4 * v + 1]);
-        acc[4 * v + 2] = fmaf(wj, x.z, acc[4 * v + 2]);
-        acc[4 * v + 3] = fmaf(wj, x.w, acc[4 * v + 3]);
+        for (int v = 0; v < 4; ++v) {
+          const uint4 x = __ldcg(src + v);
+          const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = bf16x2_to_float2(w4[e]);
+            acc[8 * v + 2 * e] = fmaf(wj, f.x, acc[8 * v + 2 * e]);
+            acc[8 * v + 2 * e + 1] = fmaf(wj, f.y, acc[8 * v + 2 * e + 1]);
+          }
+        }
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(a.o_part + off);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const float4 x = __ldcg(src + v);
+          acc[4 * v + 0] = fmaf(wj, x.x, acc[4 * v + 0]);
+          acc[4 * v + 1] = fmaf(wj, x.y, acc[4 * v + 1]);
+          acc[4 * v + 2] = fmaf(wj, x.z, acc[4 * v + 2]);
+          acc[4 * v + 3] = fmaf(wj, x.w, acc[4 * v + 3]);
+        }
       }
     }
     uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
@@ -479,15 +494,26 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (row_ok) args.lse[static_cast<size_t>(w.h) * args.lse_stride + sg.q_row0 + q_local] = lse_val;
       } else {
         const size_t prow = static_cast<size_t>(sg.slot) * args.part_rows + sg.out_row0 + q_local;
-        float* dst = args.o_part + (prow * nh + w.h) * HD;
+        const size_t off = (prow * nh + w.h) * HD;
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tO + lane_off + c * 32, o);
           tmem_wait_ld();
           reg_fence(o);
-          if (row_ok) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+          if (row_ok && args.part_bf16) {
+            uint4* d4 = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(args.o_part) + off + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 pk;
+              pk.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+              pk.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+              pk.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+              pk.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+              d4[v] = pk;
+            }
+          } else if (row_ok) {
+            float4* d4 = reinterpret_cast<float4*>(args.o_part + off + c * 32);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               d4[v] = make_float4(__uint_as_float(o[4 * v + 0]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,

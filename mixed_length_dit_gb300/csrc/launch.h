@@ -39,10 +39,11 @@ struct FwdSeg {
 struct FwdArgs {
   void* o;              // whole-sequence output [Tq][H][d] (bf16 or f32)
   float* lse;           // [H][lse_stride]
-  float* o_part;        // partial O  [P][part_rows][H][d] f32
+  float* o_part;        // partial O  [P][part_rows][H][d] f32 (bf16 elements when part_bf16)
   float* lse_part;      // partial LSE [P][H][part_rows] f32
   int32_t* counters;    // tile arrival counters, zero at launch (fused merge)
   int32_t fused_merge;  // tensor-core path: the last arriving tile merges the partials
+  int32_t part_bf16;    // tensor-core path: partial O rows in bf16
   int64_t lse_stride;   // Tq
   int64_t part_rows;    // R
   int32_t num_heads;
@@ -56,7 +57,7 @@ struct FwdArgs {
 static_assert(sizeof(FwdArgs) <= 32764, "forward arguments exceed the kernel parameter space");
 
 struct MergeArgs {
-  const float* o_part;
+  const void* o_part;   // float32, or bf16 when part_bf16
   const float* lse_part;
   void* o;
   float* lse;
@@ -66,6 +67,7 @@ struct MergeArgs {
   int32_t n_parts;
   int32_t num_heads;
   int32_t out_bf16;
+  int32_t part_bf16;
 };
 
 // Backward work: one item per (sequence, head, 128-key block); the item loops

@@ -444,11 +444,19 @@ zl_status zl_varlen_attn_fwd_workspace_size(const int32_t* cu_seqlens_q, const i
 zl_status zl_lse_merge(const float* o_partial, const float* lse_partial, int32_t n_parts, int64_t rows,
                        int32_t num_heads, int32_t head_dim, int64_t part_stride_rows, void* o,
                        int32_t out_dtype, float* lse, int64_t lse_head_stride, void* stream) {
+  return zl_lse_merge_ex(o_partial, ZL_FP32, lse_partial, n_parts, rows, num_heads, head_dim, part_stride_rows,
+                         o, out_dtype, lse, lse_head_stride, stream);
+}
+
+zl_status zl_lse_merge_ex(const void* o_partial, int32_t part_dtype, const float* lse_partial, int32_t n_parts,
+                          int64_t rows, int32_t num_heads, int32_t head_dim, int64_t part_stride_rows, void* o,
+                          int32_t out_dtype, float* lse, int64_t lse_head_stride, void* stream) {
   if (n_parts < 1 || n_parts > 64 || rows < 0 || num_heads < 1 || part_stride_rows < rows ||
       lse_head_stride < rows)
     return ZL_EINVAL;
   if (head_dim != 64 && head_dim != 128) return ZL_EUNSUPPORTED;
   if (out_dtype != ZL_BF16 && out_dtype != ZL_FP32) return ZL_EUNSUPPORTED;
+  if (part_dtype != ZL_BF16 && part_dtype != ZL_FP32) return ZL_EUNSUPPORTED;
   if (rows == 0) return ZL_OK;
   if (!o_partial || !lse_partial || !o || !lse) return ZL_EINVAL;
   if (!aligned16(o_partial) || !aligned16(o)) return ZL_EALIGN;
@@ -467,6 +475,7 @@ zl_status zl_lse_merge(const float* o_partial, const float* lse_partial, int32_t
   a.n_parts = n_parts;
   a.num_heads = num_heads;
   a.out_bf16 = out_dtype == ZL_BF16 ? 1 : 0;
+  a.part_bf16 = part_dtype == ZL_BF16 ? 1 : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return launch_counted("lse_merge", s, [&] { return zl::launch_merge(head_dim, a, sms, s); });
 }
@@ -485,8 +494,9 @@ zl_status zl_varlen_attn_fwd_ex(const void* q, const void* k, const void* v, con
                                 int32_t head_dim, int32_t dtype, float softmax_scale, const zl_tile_t* tiles,
                                 int32_t num_tiles, void* o, float* lse, void* workspace,
                                 size_t workspace_bytes, void* stream, uint32_t flags) {
-  if ((flags & ~static_cast<uint32_t>(ZL_FWD_FUSED_MERGE)) != 0) return ZL_EINVAL;
+  if ((flags & ~static_cast<uint32_t>(ZL_FWD_FUSED_MERGE | ZL_FWD_BF16_PARTIALS)) != 0) return ZL_EINVAL;
   const bool fused = (flags & ZL_FWD_FUSED_MERGE) != 0 && dtype == ZL_BF16;
+  const bool part_bf16 = (flags & ZL_FWD_BF16_PARTIALS) != 0 && dtype == ZL_BF16;
   if (dtype != ZL_BF16 && dtype != ZL_FP32) return ZL_EUNSUPPORTED;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return ZL_EINVAL;
   Plan plan;
@@ -521,6 +531,7 @@ zl_status zl_varlen_attn_fwd_ex(const void* q, const void* k, const void* v, con
     args.counters = reinterpret_cast<int32_t*>(ws + o_bytes + l_bytes);
     args.part_rows = plan.part_rows;
     args.fused_merge = fused ? 1 : 0;
+    args.part_bf16 = part_bf16 ? 1 : 0;
     if (fused) {
       st = cuda_status(cudaMemsetAsync(args.counters, 0, static_cast<size_t>(plan.n_counters) * sizeof(int32_t), s));
       if (st != ZL_OK) return st;
@@ -553,7 +564,9 @@ zl_status zl_varlen_attn_fwd_ex(const void* q, const void* k, const void* v, con
     if (fused) break;
     if (!sp.merged) continue;
     zl::MergeArgs m;
-    m.o_part = args.o_part + static_cast<size_t>(sp.rbase) * num_heads * head_dim;
+    m.o_part = static_cast<const char*>(static_cast<const void*>(args.o_part)) +
+               static_cast<size_t>(sp.rbase) * num_heads * head_dim * (part_bf16 ? 2 : 4);
+    m.part_bf16 = part_bf16 ? 1 : 0;
     m.lse_part = args.lse_part + sp.rbase;
     m.o = static_cast<char*>(o) + static_cast<size_t>(cu_seqlens_q[sp.seq]) * num_heads * head_dim * esz;
     m.lse = lse + cu_seqlens_q[sp.seq];

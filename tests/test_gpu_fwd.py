@@ -344,3 +344,61 @@ def test_concurrent_launches_on_two_streams_bitwise():
             assert torch.equal(x[4], o_ref)
             assert torch.equal(x[5], l_ref)
     zl.sync_check()
+
+
+@pytest.mark.parametrize("n,hd,fused", [(1, 64, False), (1, 128, True), (4, 128, False), (4, 128, True)])
+def test_bf16_partials(n, hd, fused):
+    """Partial O rows kept in bf16 (ZL_FWD_BF16_PARTIALS): each partial is
+    rounded once before the merge, so O stays within the bf16 tolerance of the
+    oracle and of the float32-partial result; partial LSEs stay float32, so
+    LSE is bit-identical to the float32-partial run."""
+    if n == 1:
+        wl = synth.Workload("tiny", [37, 64, 100, 256], 2, hd)
+        tiles = synth.grid_tiles(3, 256, 256, 2, 2) + synth.grid_tiles(2, 100, 100, 3, 2)
+    else:
+        wl = synth.Workload("split", [20000, 1024, 5000], 4, hd)
+        tiles = synth.grid_tiles(0, 20000, 20000, 3, 4) + synth.grid_tiles(2, 5000, 5000, 1, 3)
+    inp = synth.make_inputs(wl, seed=7, device="cuda", with_grad_out=False)
+    cu = wl.cu_seqlens()
+    o32, l32 = zl.varlen_attn_fwd(inp["q"], inp["k"], inp["v"], cu, cu, tiles=tiles, fused_merge=fused)
+    o16, l16 = zl.varlen_attn_fwd(inp["q"], inp["k"], inp["v"], cu, cu, tiles=tiles, fused_merge=fused,
+                                  bf16_partials=True)
+    zl.sync_check()
+    assert torch.equal(l16, l32)
+    assert (o16.float() - o32.float()).abs().max().item() <= TOL_O_BF16
+    # sequences that are not split over keys never touch a partial
+    assert torch.equal(o16[cu[1]:cu[2]], o32[cu[1]:cu[2]])
+    if n == 1:
+        _full_check(inp["q"], inp["k"], inp["v"], cu, cu, o16, l16, TOL_O_BF16, TOL_LSE)
+    else:
+        wl_t = synth.Workload("split", wl.seqlens, wl.num_heads, hd, splits={0: (3, 4), 2: (1, 3)})
+        _sampled_check(wl_t, inp, o16, l16, n_random=256, max_heads_long=4)
+
+
+def test_shard_mode_131k_bf16_partials():
+    """The 131,072-token sequence as 4 x 4 tiles beside 64 images, partials in
+    bf16: the oracle on sampled rows."""
+    wl = synth.config(4)
+    inp = synth.make_inputs(wl, seed=0, device="cuda", with_grad_out=False)
+    cu = wl.cu_seqlens()
+    o, lse = zl.varlen_attn_fwd(inp["q"], inp["k"], inp["v"], cu, cu, tiles=wl.tiles(), bf16_partials=True)
+    zl.sync_check()
+    _sampled_check(wl, inp, o, lse, n_random=512, max_heads_long=3)
+
+
+@pytest.mark.parametrize("hd,out_dtype,P", [(64, torch.float32, 3), (128, torch.bfloat16, 4)])
+def test_lse_merge_standalone_bf16_partials(hd, out_dtype, P):
+    """zl_lse_merge_ex on bf16 partials (3 parts: the any-count path; 4: the
+    unrolled one): the oracle's merge of the same bf16 values (widened
+    exactly), to float32 rounding."""
+    g = torch.Generator(device="cuda").manual_seed(12)
+    R, H = 513, 3
+    o_part = torch.randn((P, R, H, hd), generator=g, device="cuda").to(torch.bfloat16)
+    lse_part = 4 * torch.randn((P, H, R), generator=g, device="cuda")
+    lse_part[2, :, 5:9] = float("-inf")
+    o, lse = zl.lse_merge(o_part, lse_part, out_dtype=out_dtype)
+    zl.sync_check()
+    o_ref, l_ref = oracle.lse_merge(f64(o_part), f64(lse_part))
+    tol = TOL_O_BF16 if out_dtype == torch.bfloat16 else 1e-5
+    assert np.abs(f64(o) - o_ref).max() <= tol
+    assert np.abs(f64(lse) - l_ref).max() <= 1e-5

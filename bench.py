@@ -1,7 +1,7 @@
 """Benchmark of the coalesced varlen attention hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 1..8] [--mode step|fwd] [--seed S]
+                    [--workload 1..9] [--mode step|fwd] [--seed S]
 
 One step = one pass of the whole path over one batch: the forward over whole
 sequences and shard tiles in one launch, the exact LSE merge of the tiles, the

@@ -131,6 +131,8 @@ def config(n: int) -> Workload:
        (Ulysses degree 4: 10 heads per shard), a 480p 81-frame video as
        (2, 2, 2), another as (2, 5, 1), and 24 images of 1024 tokens whole;
        40 heads, d = 128
+    9  profiling case of the shard path and the merge: workload 6's video
+       as a 2 x 2 tile grid (float32 partials 0.8 GB, above L2)
 
     `splits` maps a sequence to (n_q, n_kv) or (n_q, n_kv, n_h) chunk counts.
     """
@@ -167,6 +169,8 @@ def config(n: int) -> Workload:
     if n == 8:
         return Workload("qhk_mix", [v720_81, v480_81, v480_81] + [img512] * 24, 40, 128,
                         splits={0: (1, 1, 4), 1: (2, 2, 2), 2: (2, 1, 5)})
+    if n == 9:
+        return Workload("video_32k_h24_split", [v480_81], 24, 128, splits={0: (2, 2)})
     raise ValueError(f"no workload {n}")
 
 

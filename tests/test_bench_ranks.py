@@ -90,7 +90,7 @@ def test_workload_descriptions_cover_every_workload():
     """Every workload bench.py can time describes itself (splits of two or
     three chunk counts) and prices its merge without error."""
     import synth
-    for n in range(1, 9):
+    for n in range(1, 10):
         wl = synth.config(n)
         desc = bench.workload_desc(wl)
         assert wl.name in desc

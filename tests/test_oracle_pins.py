@@ -370,7 +370,9 @@ def test_workload_shapes():
     wl8 = synth.config(8)
     assert wl8.total_tokens == 75600 + 2 * 32760 + 24 * 1024
     assert len(wl8.tiles()) == 4 + 8 + 10
-    for n in (4, 5, 7, 8):
+    wl9 = synth.config(9)
+    assert wl9.seqlens == synth.config(6).seqlens and len(wl9.tiles()) == 4
+    for n in (4, 5, 7, 8, 9):
         wl = synth.config(n)
         for s in wl.splits:
             ts = [t for t in wl.tiles() if t[0] == s]

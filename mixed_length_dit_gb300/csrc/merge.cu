@@ -7,7 +7,7 @@
 // bytes of each partial O row per thread (4 float32 or 8 bf16 columns), so
 // each group reads whole rows; groups are numbered head-major so the LSE reads and
 // writes of neighbouring groups are contiguous.  Grid-stride over all pairs
-// with one full wave of resident blocks.
+// with exactly one full wave of resident blocks.
 #include "common.cuh"
 #include "launch.h"
 
@@ -152,17 +152,37 @@ merge_kernel(const __grid_constant__ MergeArgs a) {
   }
 }
 
-template <int HD, bool OUT_BF16, bool PART_BF16>
-void launch_np(const MergeArgs& a, int num_sms, cudaStream_t stream) {
+// Blocks of a kernel resident per SM at once (asked once per kernel): the
+// grid is one full wave of them, so no partial second wave runs at low
+// occupancy at the end.
+template <typename K>
+int resident_blocks(K kernel) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kMergeThreads, 0) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 1;
+  }
+  return n;
+}
+
+template <int HD, int NP, bool OUT_BF16, bool PART_BF16>
+void launch_one(const MergeArgs& a, int num_sms, cudaStream_t stream) {
+  static const int per_sm = resident_blocks(merge_kernel<HD, NP, OUT_BF16, PART_BF16>);
   constexpr int kGroups = kMergeThreads / (HD / PartCols<PART_BF16>::E);
   const int64_t groups = a.rows * a.num_heads;
   const int64_t blocks_needed = (groups + kGroups - 1) / kGroups;
-  const int grid = static_cast<int>(blocks_needed < int64_t(num_sms) * 8 ? blocks_needed : int64_t(num_sms) * 8);
+  const int64_t wave = int64_t(num_sms) * per_sm;
+  const int grid = static_cast<int>(blocks_needed < wave ? blocks_needed : wave);
   if (grid <= 0) return;
+  merge_kernel<HD, NP, OUT_BF16, PART_BF16><<<grid, kMergeThreads, 0, stream>>>(a);
+}
+
+template <int HD, bool OUT_BF16, bool PART_BF16>
+void launch_np(const MergeArgs& a, int num_sms, cudaStream_t stream) {
   switch (a.n_parts) {
-    case 2: merge_kernel<HD, 2, OUT_BF16, PART_BF16><<<grid, kMergeThreads, 0, stream>>>(a); break;
-    case 4: merge_kernel<HD, 4, OUT_BF16, PART_BF16><<<grid, kMergeThreads, 0, stream>>>(a); break;
-    default: merge_kernel<HD, 0, OUT_BF16, PART_BF16><<<grid, kMergeThreads, 0, stream>>>(a); break;
+    case 2: launch_one<HD, 2, OUT_BF16, PART_BF16>(a, num_sms, stream); break;
+    case 4: launch_one<HD, 4, OUT_BF16, PART_BF16>(a, num_sms, stream); break;
+    default: launch_one<HD, 0, OUT_BF16, PART_BF16>(a, num_sms, stream); break;
   }
 }
 

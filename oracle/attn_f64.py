@@ -353,3 +353,26 @@ def dkdv_rows(q, k, v, do, cu_q, cu_k, seq, head, kv_rows, scale=None):
     ds = grad_scores(p, dp, dsum)
     dk = grad_k(ds, qq, scale)
     return dk, dv
+
+
+def grads_one_query_row(q, k, v, do_row, cu_q, cu_k, seq, head, row, scale=None):
+    """Gradients of one head of sequence `seq` when dO is zero except at query
+    row `row` (relative to the sequence), where it is `do_row` [d].
+
+    Then D = rowsum(dO * O) and dP = dO V^T vanish on every other row, so dS is
+    zero there and only that row's softmax enters:
+      dV_j = P_rj dO_r,   dK_j = scale * dS_rj q_r,   dQ_r = scale * dS_r K,
+    with dS_r = P_r * (dO_r V^T - dO_r . O_r); every other dQ row is zero.
+    Returns (dq_row [d], dk [Lk, d], dv [Lk, d])."""
+    d = q.shape[2]
+    if scale is None:
+        scale = default_scale(d)
+    qa = int(cu_q[seq])
+    ka, kb = int(cu_k[seq]), int(cu_k[seq + 1])
+    qr = q[qa + row:qa + row + 1, head]
+    dor = np.asarray(do_row, dtype=np.float64)[None, :]
+    kk, vv = k[ka:kb, head], v[ka:kb, head]
+    o_r, lse_r = attention_f64(qr, kk, vv, scale)
+    p = probabilities(scores(qr, kk, scale), lse_r)
+    ds = grad_scores(p, dor @ vv.T, (dor * o_r).sum(axis=1))
+    return grad_q(ds, kk, scale)[0], grad_k(ds, qr, scale), grad_v(p, dor)

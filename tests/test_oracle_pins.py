@@ -310,11 +310,32 @@ def pin_row_helpers():
     assert np.allclose(dvr, dv[20 + np.array(rows), 1], atol=1e-12)
 
 
+def pin_one_query_row():
+    """With dO zero except at one query row, the full backward (itself pinned
+    by finite differences) gives exactly the one-row gradients: dK and dV of
+    every key of that sequence and head, dQ of that row, and zero dQ on every
+    other row."""
+    q, k, v, cu = _packed([9, 300, 17], 3, 8, seed=18)
+    do_full = _rng(19).standard_normal(q.shape)
+    for s, h, r in ((1, 2, 0), (1, 0, 173), (2, 1, 16), (0, 1, 4)):
+        a, b = cu[s], cu[s + 1]
+        do = np.zeros_like(do_full)
+        do[a + r, h] = do_full[a + r, h]
+        dq, dk, dv = oracle.varlen_attn_bwd(q, k, v, do, cu, cu)
+        dq_r, dk_s, dv_s = oracle.grads_one_query_row(q, k, v, do[a + r, h], cu, cu, s, h, r)
+        assert np.allclose(dq[a + r, h], dq_r, atol=1e-13)
+        assert np.allclose(dk[a:b, h], dk_s, atol=1e-13)
+        assert np.allclose(dv[a:b, h], dv_s, atol=1e-13)
+        mask = np.ones(q.shape[0], dtype=bool)
+        mask[a + r] = False
+        assert np.all(dq[mask, h] == 0) and np.all(dq[:, [x for x in range(3) if x != h]] == 0)
+
+
 PINS = [pin_length_one, pin_constant_keys, pin_identical_values,
         pin_two_keys_closed_form, pin_brute_force_tiny, pin_scipy_softmax,
         pin_merge_equals_unsplit, pin_head_sharded_configurations, pin_merge_empty_parts,
         pin_finite_differences,
-        pin_gradient_sums, pin_sequence_isolation_and_order, pin_row_helpers]
+        pin_gradient_sums, pin_sequence_isolation_and_order, pin_row_helpers, pin_one_query_row]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -470,9 +491,24 @@ def _mut_tile_heads_from_zero(tile, num_heads):
     return list(range(num_heads))
 
 
+def _mut_one_row_no_d(q, k, v, do_row, cu_q, cu_k, seq, head, row, scale=None):
+    # the one-row gradients with the D = dO . O term of dS dropped
+    d = q.shape[2]
+    scale = of.default_scale(d) if scale is None else scale
+    qa = int(cu_q[seq])
+    ka, kb = int(cu_k[seq]), int(cu_k[seq + 1])
+    qr = q[qa + row:qa + row + 1, head]
+    dor = np.asarray(do_row, dtype=np.float64)[None, :]
+    kk, vv = k[ka:kb, head], v[ka:kb, head]
+    _, lse_r = of.attention_f64(qr, kk, vv, scale)
+    p = of.probabilities(of.scores(qr, kk, scale), lse_r)
+    ds = p * (dor @ vv.T)
+    return scale * (ds @ kk)[0], scale * (ds.T @ qr), p.T @ dor
+
+
 _REAL = {name: getattr(of, name) for name in
          ("scores", "row_logsumexp", "probabilities", "lse_merge", "grad_scores",
-          "grad_q", "grad_k", "grad_v", "tile_heads")}
+          "grad_q", "grad_k", "grad_v", "tile_heads", "grads_one_query_row")}
 
 MUTATIONS = [
     ("scores", _mut_no_scale), ("scores", _mut_inverse_scale),
@@ -483,6 +519,7 @@ MUTATIONS = [
     ("grad_scores", _mut_grad_scores_no_d), ("grad_scores", _mut_grad_scores_sign),
     ("grad_q", _mut_grad_q_no_scale), ("grad_k", _mut_grad_k_no_transpose),
     ("grad_v", _mut_grad_v_wrong_side), ("tile_heads", _mut_tile_heads_from_zero),
+    ("grads_one_query_row", _mut_one_row_no_d),
 ]
 
 

@@ -171,3 +171,85 @@ def test_concurrent_launches_on_two_streams():
             assert torch.equal(dk, r[1]) and torch.equal(dv, r[2])
             assert (dq.float() - r[0].float()).abs().max().item() <= 1e-2 * r[0].float().abs().max().item()
     zl.sync_check()
+
+
+def _sampled_grad_check(wl, inp, cu, grads, checks, n_random=256, seed=1):
+    dq, dk, dv = grads
+    rng = np.random.default_rng(seed)
+    for s, h in checks:
+        L = wl.seqlens[s]
+        a, b = cu[s], cu[s + 1]
+        rows = sample_rows(L, synth.chunk_bounds(L, wl.splits.get(s, (1, 1))[0]), n_random, rng)
+        qs, ks, vs, dos = (f64(inp[n][a:b]) for n in ("q", "k", "v", "do"))
+        cu1 = [0, L]
+        dq_ref = oracle.dq_rows(qs, ks, vs, dos, cu1, cu1, 0, h, rows)
+        dk_ref, dv_ref = oracle.dkdv_rows(qs, ks, vs, dos, cu1, cu1, 0, h, rows)
+        for name, got, ref in (("dq", dq, dq_ref), ("dk", dk, dk_ref), ("dv", dv, dv_ref)):
+            e = rel_l2(f64(got[a:b][rows, h]), ref)
+            assert e <= TOL_GRAD_REL_L2, (s, h, name, e)
+
+
+def test_wan_mix_sampled():
+    """Wan mix (32,760- and 14,040-token videos, 1,024- and 4,096-token images,
+    40 heads): dQ, dK and dV rows sampled on one head per sequence kind."""
+    wl = synth.config(3)
+    inp = synth.make_inputs(wl, seed=0, device="cuda")
+    cu = wl.cu_seqlens()
+    grads = _fwd_bwd(inp["q"], inp["k"], inp["v"], inp["do"], cu, cu)
+    _sampled_grad_check(wl, inp, cu, grads, [(0, 5), (1, 39), (3, 12), (30, 27)])
+
+
+def test_shard_mode_131k_dense():
+    """131,072-token sequence (run as 4 x 4 tiles in the forward) beside 64
+    images, dense dO: dQ rows of the long sequence sampled on two heads, every
+    gradient of two images on one head each, and on every head of the long
+    sequence the identity sum_j dV_j = sum_i dO_i (rows of P sum to one)."""
+    wl = synth.config(4)
+    inp = synth.make_inputs(wl, seed=0, device="cuda")
+    cu = wl.cu_seqlens()
+    dq, dk, dv = _fwd_bwd(inp["q"], inp["k"], inp["v"], inp["do"], cu, cu, wl.tiles())
+    L = wl.seqlens[0]
+    rng = np.random.default_rng(2)
+    rows = sample_rows(L, synth.chunk_bounds(L, 4), 256, rng)
+    for h in (0, 33):
+        qs, ks, vs, dos = (f64(inp[n][:L, h:h + 1]) for n in ("q", "k", "v", "do"))   # one head
+        ref = oracle.dq_rows(qs, ks, vs, dos, [0, L], [0, L], 0, 0, rows)
+        e = rel_l2(f64(dq[rows, h]), ref)
+        assert e <= TOL_GRAD_REL_L2, (h, e)
+    _sampled_grad_check(wl, inp, cu, (dq, dk, dv), [(1, 7), (64, 39)], n_random=1024)
+    # bf16 rounding of P and of dV (2^-9 relative per entry, random in sign)
+    # leaves the identity's relative error near 1e-5
+    sv = dv[:L].double().sum(dim=0)
+    so = inp["do"][:L].double().sum(dim=0)
+    e = ((sv - so).norm() / so.norm()).item()
+    assert e <= 1e-3, e
+
+
+def test_shard_mode_131k_one_query_row():
+    """The same batch with dO zero except one query row of the long sequence on
+    three heads: dK and dV of all 131,072 keys of those heads come from that
+    row's softmax alone and are checked exactly, as is dQ of the row; every
+    other dQ row, and every gradient of the other heads and sequences, is
+    zero."""
+    wl = synth.config(4)
+    inp = synth.make_inputs(wl, seed=1, device="cuda")
+    cu = wl.cu_seqlens()
+    L = wl.seqlens[0]
+    picks = {0: 0, 17: 65535, 39: 131071}            # head -> query row
+    do = torch.zeros_like(inp["do"])
+    for h, r in picks.items():
+        do[r, h] = inp["do"][r, h]
+    dq, dk, dv = _fwd_bwd(inp["q"], inp["k"], inp["v"], do, cu, cu, wl.tiles())
+    for h, r in picks.items():
+        qs, ks, vs = (f64(inp[n][:L, h:h + 1]) for n in ("q", "k", "v"))            # one head
+        dq_r, dk_ref, dv_ref = oracle.grads_one_query_row(qs, ks, vs, f64(do[r, h]), [0, L], [0, L], 0, 0, r)
+        for name, got, ref in (("dq", dq[r, h], dq_r), ("dk", dk[:L, h], dk_ref), ("dv", dv[:L, h], dv_ref)):
+            e = rel_l2(f64(got), ref)
+            assert e <= TOL_GRAD_REL_L2, (h, name, e)
+        others = torch.ones(dq.shape[0], dtype=torch.bool, device="cuda")
+        others[r] = False
+        assert torch.count_nonzero(dq[others, h]).item() == 0
+    quiet = [h for h in range(wl.num_heads) if h not in picks]
+    for g in (dq, dk, dv):
+        assert torch.count_nonzero(g[:, quiet]).item() == 0
+        assert torch.count_nonzero(g[L:]).item() == 0

@@ -253,3 +253,30 @@ def test_shard_mode_131k_one_query_row():
     for g in (dq, dk, dv):
         assert torch.count_nonzero(g[:, quiet]).item() == 0
         assert torch.count_nonzero(g[L:]).item() == 0
+
+
+def test_fig2_mix_dense():
+    """The Fig. 2 batch (three 147,600-token videos, run as 2 x 2 tiles in the
+    forward, beside 228 images of 3,600 tokens; 12 heads), dense dO: dQ rows of
+    one video sampled on two heads, every gradient of two images on one head
+    each, and for each video on every head sum_j dV_j = sum_i dO_i."""
+    wl = synth.config(7)
+    inp = synth.make_inputs(wl, seed=0, device="cuda")
+    cu = wl.cu_seqlens()
+    dq, dk, dv = _fwd_bwd(inp["q"], inp["k"], inp["v"], inp["do"], cu, cu, wl.tiles())
+    L = wl.seqlens[1]
+    a = cu[1]
+    rng = np.random.default_rng(3)
+    rows = sample_rows(L, synth.chunk_bounds(L, 2), 256, rng)
+    for h in (0, 11):
+        qs, ks, vs, dos = (f64(inp[n][a:a + L, h:h + 1]) for n in ("q", "k", "v", "do"))
+        ref = oracle.dq_rows(qs, ks, vs, dos, [0, L], [0, L], 0, 0, rows)
+        e = rel_l2(f64(dq[a:a + L][rows, h]), ref)
+        assert e <= TOL_GRAD_REL_L2, (h, e)
+    _sampled_grad_check(wl, inp, cu, (dq, dk, dv), [(3, 4), (230, 9)], n_random=1024)
+    for s in range(3):
+        x, y = cu[s], cu[s + 1]
+        sv = dv[x:y].double().sum(dim=0)
+        so = inp["do"][x:y].double().sum(dim=0)
+        e = ((sv - so).norm() / so.norm()).item()
+        assert e <= 1e-3, (s, e)

@@ -177,6 +177,24 @@ def test_merge_argument_checks(lib):
     assert lib.zl_lse_merge(p, p, 2, 10, 2, 64, 5, p, 0, p, 10, None) == _lib.ZL_EINVAL
     assert lib.zl_lse_merge(p, p, 2, 10, 2, 32, 10, p, 0, p, 10, None) == _lib.ZL_EUNSUPPORTED
     assert lib.zl_lse_merge(p, p, 2, 0, 2, 64, 0, p, 0, p, 0, None) == _lib.ZL_OK
+    # the partial dtype of zl_lse_merge_ex: bf16 or float32 only
+    assert lib.zl_lse_merge_ex(p, 7, p, 2, 10, 2, 64, 10, p, 0, p, 10, None) == _lib.ZL_EUNSUPPORTED
+    assert lib.zl_lse_merge_ex(p, _lib.ZL_BF16, p, 0, 10, 2, 64, 10, p, 0, p, 10, None) == _lib.ZL_EINVAL
+    assert lib.zl_lse_merge_ex(p, _lib.ZL_BF16, p, 2, 0, 2, 64, 0, p, 0, p, 0, None) == _lib.ZL_OK
+
+
+def test_forward_flags(lib):
+    """zl_varlen_attn_fwd_ex accepts exactly the documented flag bits.  The
+    head dimension 96 is unsupported, which the library reports only after the
+    flags have passed, so no call here can reach a launch."""
+    cq, nq = _lib.int32_array([0, 5])
+    p = ctypes.c_void_p(64)
+    args = [p, p, p, cq, cq, nq - 1, 2, 96, _lib.ZL_BF16, 0.125, None, 0, p, p, None, 0, None]
+    assert lib.zl_varlen_attn_fwd_ex(*args, 4) == _lib.ZL_EINVAL
+    assert lib.zl_varlen_attn_fwd_ex(*args, 1 << 31) == _lib.ZL_EINVAL
+    for ok_flags in (0, _lib.ZL_FWD_FUSED_MERGE, _lib.ZL_FWD_BF16_PARTIALS,
+                     _lib.ZL_FWD_FUSED_MERGE | _lib.ZL_FWD_BF16_PARTIALS):
+        assert lib.zl_varlen_attn_fwd_ex(*args, ok_flags) == _lib.ZL_EUNSUPPORTED
 
 
 def test_bwd_argument_checks(lib):

@@ -31,8 +31,12 @@
  *     zl_sync_check().
  *   - Every entry point returns a zl_status (0 = success, < 0 = error) and
  *     never aborts the process.
- *   - Thread-safe; the only global state is a per-device cache of device
- *     attributes and a process-wide launch counter.
+ *   - Thread-safe.  Global state: a per-device cache of device attributes
+ *     (SM count, the merge kernels' resident blocks per SM), a process-wide
+ *     launch counter, the optional profiling hook (zl_profile_*), one device
+ *     error word per kernel family (set by a kernel that gave up a wait, read
+ *     and cleared by zl_sync_check) and zl_varlen_attn_bwd_static's scratch
+ *     array.
  */
 #ifndef ZL_ATTN_H
 #define ZL_ATTN_H
@@ -109,7 +113,9 @@ int32_t zl_version(void);
  * sequence is split along its keys).  It holds the float32 shard partials:
  * for the sequences with n_kv_chunks > 1 (in sequence order, R = sum of their
  * query lengths, P = largest n_kv_chunks) an O partial [P][R][H][d] and an
- * LSE partial [P][H][R], then the fused-merge arrival counters.
+ * LSE partial [P][H][R], then the fused-merge arrival counters.  Under
+ * ZL_FWD_BF16_PARTIALS the O partial holds bf16 elements in the first half
+ * of the same region; the size is the same.
  * Same argument rules as zl_varlen_attn_fwd.  Writes the size to *bytes.
  */
 zl_status zl_varlen_attn_fwd_workspace_size(

@@ -136,10 +136,12 @@ class ClockSampler:
             return None
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows),
+                "power_w": round(statistics.median(pw), 1) if pw else None}
 
 
 def gpu_index_for_smi(local_rank: int) -> str:
@@ -391,6 +393,7 @@ def main():
         barrier()
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
+        e2e_sampler = ClockSampler(gpu_index_for_smi(local_rank))
         f0.record(comp)
         h2d.wait_event(f0)
         for i in range(k_e2e):
@@ -398,6 +401,7 @@ def main():
         comp.wait_stream(d2h)
         f1.record(comp)
         torch.cuda.synchronize()
+        e2e_clocks = e2e_sampler.stop()
         barrier()
         ems = reduce_max_ms(f0.elapsed_time(f1), world, dev)
         bi = sum(t.numel() * t.element_size() for t in host_in.values())
@@ -405,7 +409,8 @@ def main():
         e2e = {"value": round(job_tflops(world, k_e2e, flops_step, ems), 1),
                "unit": "TFLOP/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": k_e2e,
                "ms_per_step": round(ems / k_e2e, 3),
-               "note": "copies of neighbouring steps overlap compute (2 copy streams, double-buffered device tensors)"}
+               "note": "copies of neighbouring steps overlap compute (2 copy streams, double-buffered device tensors)",
+               "clocks": e2e_clocks}
         del dev_in, dev_out, host_in, host_out, lse2
 
     # ---------------- CPU oracle baseline (rank 0, single GPU)

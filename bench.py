@@ -103,7 +103,8 @@ class ClockSampler:
     """nvidia-smi clock and throttle-reason samples every 200 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "temperature.gpu,clocks.mem")
 
     def __init__(self, gpu_index: str):
         self.path = tempfile.mktemp(prefix="zl_clocks_", suffix=".csv")
@@ -137,11 +138,14 @@ class ClockSampler:
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        tc = [float(r[9]) for r in rows if len(r) > 9 and r[9].replace(".", "").isdigit()]
+        mem = [float(r[10]) for r in rows if len(r) > 10 and r[10].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(rows),
-                "power_w": round(statistics.median(pw), 1) if pw else None}
+                "power_w": round(statistics.median(pw), 1) if pw else None,
+                "temp_c": max(tc) if tc else None, "mem_mhz": statistics.median(mem) if mem else None}
 
 
 def gpu_index_for_smi(local_rank: int) -> str:

@@ -103,10 +103,10 @@ def test_train_step_sampled():
         L = wl.seqlens[s]
         a, b = cu[s], cu[s + 1]
         rows = sample_rows(L, synth.chunk_bounds(L, wl.splits.get(s, (1, 1))[0]), 256, rng)
-        qs, ks, vs, dos = (f64(inp[n][a:b]) for n in ("q", "k", "v", "do"))
+        qs, ks, vs, dos = (f64(inp[n][a:b, h:h + 1]) for n in ("q", "k", "v", "do"))   # one head
         cu1 = [0, L]
-        dq_ref = oracle.dq_rows(qs, ks, vs, dos, cu1, cu1, 0, h, rows)
-        dk_ref, dv_ref = oracle.dkdv_rows(qs, ks, vs, dos, cu1, cu1, 0, h, rows)
+        dq_ref = oracle.dq_rows(qs, ks, vs, dos, cu1, cu1, 0, 0, rows)
+        dk_ref, dv_ref = oracle.dkdv_rows(qs, ks, vs, dos, cu1, cu1, 0, 0, rows)
         for name, got, ref in (("dq", dq, dq_ref), ("dk", dk, dk_ref), ("dv", dv, dv_ref)):
             e = rel_l2(f64(got[a:b][rows, h]), ref)
             assert e <= TOL_GRAD_REL_L2, (s, h, name, e)
@@ -180,10 +180,10 @@ def _sampled_grad_check(wl, inp, cu, grads, checks, n_random=256, seed=1):
         L = wl.seqlens[s]
         a, b = cu[s], cu[s + 1]
         rows = sample_rows(L, synth.chunk_bounds(L, wl.splits.get(s, (1, 1))[0]), n_random, rng)
-        qs, ks, vs, dos = (f64(inp[n][a:b]) for n in ("q", "k", "v", "do"))
+        qs, ks, vs, dos = (f64(inp[n][a:b, h:h + 1]) for n in ("q", "k", "v", "do"))   # one head
         cu1 = [0, L]
-        dq_ref = oracle.dq_rows(qs, ks, vs, dos, cu1, cu1, 0, h, rows)
-        dk_ref, dv_ref = oracle.dkdv_rows(qs, ks, vs, dos, cu1, cu1, 0, h, rows)
+        dq_ref = oracle.dq_rows(qs, ks, vs, dos, cu1, cu1, 0, 0, rows)
+        dk_ref, dv_ref = oracle.dkdv_rows(qs, ks, vs, dos, cu1, cu1, 0, 0, rows)
         for name, got, ref in (("dq", dq, dq_ref), ("dk", dk, dk_ref), ("dv", dv, dv_ref)):
             e = rel_l2(f64(got[a:b][rows, h]), ref)
             assert e <= TOL_GRAD_REL_L2, (s, h, name, e)

@@ -1,7 +1,8 @@
 """Benchmark of the coalesced varlen attention hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload 1..9] [--mode step|fwd] [--seed S]
+                    [--workload 1..9] [--mode step|fwd] [--seed S] [--bf16-partials]
+                    [--no-e2e] [--no-cpu-baseline]
 
 One step = one pass of the whole path over one batch: the forward over whole
 sequences and shard tiles in one launch, the exact LSE merge of the tiles, the
@@ -21,6 +22,16 @@ maximum over ranks and the value is the work of all ranks over that time.
 
 --impl reference times the float64 CPU oracle (the correctness reference) on a
 bounded sample of the same workload, on rank 0 only.
+
+Besides the metric the JSON line carries: the per-kernel launch times of the
+timed region (the library's event hook), the dominant kernel's roofline
+(algorithmic FLOPs or bytes per launch over its mean launch time, against the
+measured peak, with the DRAM bytes of the last ncu capture of the same kernel
+source), the oracle's CPU throughput on a bounded sample, an end-to-end leg
+(pinned host inputs in and all results out inside the timed region) with its
+own clock record, the number of library launches, and the SM clock, power,
+temperature and throttle reasons sampled while each timed region ran.
+--bf16-partials keeps the partial rows of key-split sequences in bf16.
 """
 from __future__ import annotations
 

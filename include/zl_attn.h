@@ -123,6 +123,37 @@ zl_status zl_varlen_attn_fwd_workspace_size(
     int32_t num_heads, int32_t head_dim, const zl_tile_t* tiles, int32_t num_tiles,
     size_t* bytes);
 
+/* One work item of the forward, as zl_varlen_attn_fwd_schedule reports it. */
+typedef struct {
+  int32_t launch;   /* forward launch of the call that runs it (a call with more
+                       segments than one launch's parameters hold makes several) */
+  int32_t seq;      /* sequence index                                          */
+  int32_t tile;     /* index into the caller's tile table; -1: the whole sequence */
+  int32_t head;     /* head                                                     */
+  int32_t q_start;  /* first query row, relative to the sequence                */
+  int32_t q_len;    /* query rows (up to 256 for ZL_BF16, 128 for ZL_FP32)      */
+  int32_t k_start;  /* first key of the rows' key range, relative to the sequence */
+  int32_t k_len;    /* keys every row of the item attends to                    */
+} zl_work_item_t;
+
+/*
+ * The forward's work items for this batch, host only (no device work): the
+ * tile scheduler of the Coalesced Attention Engine (Zellige §IV-D orders the
+ * call's segments stably; §IV-C fills in decreasing price) as this library
+ * applies it on one GPU.  Segments -- whole sequences and tiles -- are stably
+ * ordered by decreasing key count (ties in input order); each splits into
+ * items head by head, query block fastest; items run in this order, every SM
+ * taking the next one when it is ready.  Writes the first max_items items to
+ * `items` (host; may be NULL when max_items is 0) and their total to
+ * *n_items.  Same argument rules and errors as zl_varlen_attn_fwd; `dtype`
+ * selects the item size (256 query rows for ZL_BF16, 128 for ZL_FP32).
+ */
+zl_status zl_varlen_attn_fwd_schedule(
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
+    int32_t num_heads, int32_t head_dim, int32_t dtype,
+    const zl_tile_t* tiles, int32_t num_tiles,
+    zl_work_item_t* items, int64_t max_items, int64_t* n_items);
+
 /*
  * Forward of the coalesced block-diagonal attention (Zellige §IV-D).
  *

@@ -61,6 +61,24 @@ def bwd_workspace_bytes(cu_seqlens_q, cu_seqlens_k, num_heads, head_dim) -> int:
     return int(out.value)
 
 
+def fwd_schedule(cu_seqlens_q, cu_seqlens_k, num_heads, head_dim, tiles=None, dtype=torch.bfloat16):
+    """The forward's work items in launch order (host only): a list of
+    (launch, seq, tile, head, q_start, q_len, k_start, k_len) tuples, tile
+    -1 for a whole sequence (zl_varlen_attn_fwd_schedule)."""
+    lib = _lib.load()
+    cq, nq = _lib.int32_array(cu_seqlens_q)
+    ck, _ = _lib.int32_array(cu_seqlens_k)
+    ta, nt = _lib.tile_array(tiles)
+    code = _lib.ZL_BF16 if dtype == torch.bfloat16 else _lib.ZL_FP32
+    n = ctypes.c_int64(0)
+    _lib.check(lib.zl_varlen_attn_fwd_schedule(cq, ck, nq - 1, num_heads, head_dim, code, ta, nt, None, 0,
+                                               ctypes.byref(n)), "zl_varlen_attn_fwd_schedule")
+    arr = (_lib.WorkItem * max(1, n.value))()
+    _lib.check(lib.zl_varlen_attn_fwd_schedule(cq, ck, nq - 1, num_heads, head_dim, code, ta, nt, arr, n.value,
+                                               ctypes.byref(n)), "zl_varlen_attn_fwd_schedule")
+    return [tuple(getattr(arr[i], f) for f, _ in _lib.WorkItem._fields_) for i in range(n.value)]
+
+
 def alloc_workspace(nbytes: int, device) -> torch.Tensor | None:
     if nbytes == 0:
         return None

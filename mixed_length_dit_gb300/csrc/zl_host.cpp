@@ -188,6 +188,7 @@ struct Plan {
   std::vector<int> split_index;     // per sequence: -1, or index into splits
   std::vector<SplitSeq> splits;
   std::vector<zl_tile_t> tiles;     // sorted by (seq, h_chunk, q_chunk, kv_chunk), h_len resolved
+  std::vector<int32_t> tile_src;    // index of each sorted tile in the caller's table
   int64_t part_rows = 0;            // R
   int n_parts = 0;                  // P
   int64_t n_counters = 0;           // arrival counters: (query chunk, 128-row block) x head
@@ -240,12 +241,22 @@ zl_status make_plan(const int32_t* cu_q, const int32_t* cu_k, int32_t b, int32_t
     if (t.h_start < 0 || t.h_len < 1 || int64_t(t.h_start) + t.h_len > nh) return ZL_EINVAL;
     if (t.h_chunk < 0 || t.h_chunk >= nh) return ZL_EINVAL;
   }
-  std::stable_sort(plan->tiles.begin(), plan->tiles.end(), [](const zl_tile_t& a, const zl_tile_t& c) {
+  plan->tile_src.resize(plan->tiles.size());
+  for (size_t x = 0; x < plan->tile_src.size(); ++x) plan->tile_src[x] = static_cast<int32_t>(x);
+  std::stable_sort(plan->tile_src.begin(), plan->tile_src.end(), [&](int32_t ia, int32_t ic) {
+    const zl_tile_t& a = plan->tiles[static_cast<size_t>(ia)];
+    const zl_tile_t& c = plan->tiles[static_cast<size_t>(ic)];
     if (a.seq != c.seq) return a.seq < c.seq;
     if (a.h_chunk != c.h_chunk) return a.h_chunk < c.h_chunk;
     if (a.q_chunk != c.q_chunk) return a.q_chunk < c.q_chunk;
     return a.kv_chunk < c.kv_chunk;
   });
+  {
+    std::vector<zl_tile_t> sorted;
+    sorted.reserve(plan->tiles.size());
+    for (int32_t x : plan->tile_src) sorted.push_back(plan->tiles[static_cast<size_t>(x)]);
+    plan->tiles.swap(sorted);
+  }
   // Each split sequence: a full n_h x n_q x n_kv grid.  Head chunk 0's tiles
   // are an n_q x n_kv grid partitioning the query range and the key range
   // into contiguous chunks in chunk order; every further head chunk repeats
@@ -337,6 +348,8 @@ struct Segment {
   FwdSeg seg;
   int64_t cost;   // keys visited per query block
   int order;      // input order (sequence index, then tile order)
+  int32_t seq;    // the segment's sequence
+  int32_t tile;   // index in the caller's tile table, or -1: the whole sequence
 };
 
 // Whole sequences and tiles as segments, stably ordered by decreasing cost.
@@ -355,6 +368,8 @@ std::vector<Segment> schedule_fwd(const Plan& p, const int32_t* cu_q, const int3
       g.seg = FwdSeg{cu_q[s], cu_k[s], lq, lk, cu_q[s], -1, 0, 0, 0, 0, nh};
       g.cost = lk;
       g.order = order++;
+      g.seq = s;
+      g.tile = -1;
       segs.push_back(g);
     } else {
       const SplitSeq& sp = p.splits[static_cast<size_t>(si)];
@@ -373,6 +388,8 @@ std::vector<Segment> schedule_fwd(const Plan& p, const int32_t* cu_q, const int3
         }
         g.cost = t.k_len;
         g.order = order++;
+        g.seq = s;
+        g.tile = p.tile_src[ti];
         segs.push_back(g);
       }
     }
@@ -438,6 +455,48 @@ zl_status zl_varlen_attn_fwd_workspace_size(const int32_t* cu_seqlens_q, const i
                                  num_tiles, &plan);
   if (st != ZL_OK) return st;
   *bytes = fwd_workspace_bytes(plan, num_heads, head_dim);
+  return ZL_OK;
+}
+
+zl_status zl_varlen_attn_fwd_schedule(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
+                                      int32_t num_heads, int32_t head_dim, int32_t dtype, const zl_tile_t* tiles,
+                                      int32_t num_tiles, zl_work_item_t* items, int64_t max_items,
+                                      int64_t* n_items) {
+  if (!n_items || max_items < 0 || (max_items > 0 && !items)) return ZL_EINVAL;
+  if (dtype != ZL_BF16 && dtype != ZL_FP32) return ZL_EUNSUPPORTED;
+  Plan plan;
+  const zl_status st = make_plan(cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, tiles, num_tiles, &plan);
+  if (st != ZL_OK) return st;
+  const std::vector<Segment> segs = schedule_fwd(plan, cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads);
+  const int rows = dtype == ZL_BF16 ? zl::kFwdRowsPerItem : kBlockM;
+  // the numbering of fill_args and the kernels' decode: launch by launch,
+  // segment by segment, head-major, query block fastest
+  int64_t n = 0;
+  int32_t launch = 0;
+  for (size_t first = 0; first < segs.size(); first += kMaxSegs, ++launch) {
+    const size_t last = std::min(segs.size(), first + kMaxSegs);
+    for (size_t i = first; i < last; ++i) {
+      const Segment& g = segs[i];
+      const FwdSeg& s = g.seg;
+      const int32_t q0 = s.q_row0 - cu_seqlens_q[g.seq];
+      const int32_t k0 = s.k_row0 - cu_seqlens_k[g.seq];
+      const int32_t nqb = (s.q_len + rows - 1) / rows;
+      for (int32_t h = s.h0; h < s.h0 + s.nh; ++h)
+        for (int32_t qb = 0; qb < nqb; ++qb, ++n) {
+          if (n >= max_items) continue;
+          zl_work_item_t& w = items[n];
+          w.launch = launch;
+          w.seq = g.seq;
+          w.tile = g.tile;
+          w.head = h;
+          w.q_start = q0 + qb * rows;
+          w.q_len = std::min(rows, s.q_len - qb * rows);
+          w.k_start = k0;
+          w.k_len = s.k_len;
+        }
+    }
+  }
+  *n_items = n;
   return ZL_OK;
 }
 

@@ -263,6 +263,33 @@ zl_status zl_varlen_attn_bwd_workspace_size(
     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
     int32_t num_heads, int32_t head_dim, size_t* bytes);
 
+/* One work item of the backward, as zl_varlen_attn_bwd_schedule reports it. */
+typedef struct {
+  int32_t launch;   /* backward launch of the call that runs it                */
+  int32_t seq;      /* sequence index                                          */
+  int32_t head;     /* head                                                     */
+  int32_t k_start;  /* first key of the item's key block, relative to the sequence */
+  int32_t k_len;    /* keys of the block (up to 128)                            */
+  int32_t q_len;    /* query rows the block visits: all of the sequence's       */
+} zl_bwd_work_item_t;
+
+/*
+ * The backward's work items for this batch, host only (no device work).
+ * The backward of a split sequence is the sum over its tiles, i.e. the
+ * backward of the whole sequence, so every sequence runs whole; sequences
+ * are stably ordered by decreasing query count (the rows each of their key
+ * blocks visits), each splits into 128-key blocks head by head, key block
+ * fastest, and the items run in this order, every SM taking the next one
+ * when it is ready.  Writes the first max_items items to `items` (host; may
+ * be NULL when max_items is 0) and their total to *n_items.  Same argument
+ * rules and errors as zl_varlen_attn_bwd's batch description (cu_seqlens,
+ * heads, head_dim, tiles).
+ */
+zl_status zl_varlen_attn_bwd_schedule(
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
+    int32_t num_heads, int32_t head_dim, const zl_tile_t* tiles, int32_t num_tiles,
+    zl_bwd_work_item_t* items, int64_t max_items, int64_t* n_items);
+
 /*
  * Backward of zl_varlen_attn_fwd: the analytic gradient of
  * O = softmax(Q K^T * scale) V per sequence and head (the paper trains with

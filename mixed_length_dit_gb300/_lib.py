@@ -29,7 +29,7 @@ EXPORTS = (
     "zl_status_string", "zl_version", "zl_varlen_attn_fwd_workspace_size", "zl_varlen_attn_fwd",
     "zl_lse_merge", "zl_varlen_attn_bwd_workspace_size", "zl_varlen_attn_bwd", "zl_sync_check",
     "zl_launch_count", "zl_profile_begin", "zl_profile_end", "zl_varlen_attn_bwd_static",
-    "zl_varlen_attn_fwd_ex", "zl_lse_merge_ex", "zl_varlen_attn_fwd_schedule",
+    "zl_varlen_attn_fwd_ex", "zl_lse_merge_ex", "zl_varlen_attn_fwd_schedule", "zl_varlen_attn_bwd_schedule",
 )
 
 ZL_FWD_FUSED_MERGE = 1
@@ -40,6 +40,11 @@ class WorkItem(ctypes.Structure):
     """zl_work_item_t"""
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("launch", "seq", "tile", "head", "q_start", "q_len", "k_start", "k_len")]
+
+
+class BwdWorkItem(ctypes.Structure):
+    """zl_bwd_work_item_t"""
+    _fields_ = [(n, ctypes.c_int32) for n in ("launch", "seq", "head", "k_start", "k_len", "q_len")]
 
 
 class Tile(ctypes.Structure):
@@ -97,6 +102,9 @@ def load() -> ctypes.CDLL:
     lib.zl_varlen_attn_fwd_schedule.restype = c_i32
     lib.zl_varlen_attn_fwd_schedule.argtypes = [i32p, i32p, c_i32, c_i32, c_i32, c_i32, tilep, c_i32,
                                                 ctypes.POINTER(WorkItem), c_i64, ctypes.POINTER(c_i64)]
+    lib.zl_varlen_attn_bwd_schedule.restype = c_i32
+    lib.zl_varlen_attn_bwd_schedule.argtypes = [i32p, i32p, c_i32, c_i32, c_i32, tilep, c_i32,
+                                                ctypes.POINTER(BwdWorkItem), c_i64, ctypes.POINTER(c_i64)]
     lib.zl_lse_merge_ex.restype = c_i32
     lib.zl_lse_merge_ex.argtypes = [vp, c_i32, vp, c_i32, c_i64, c_i32, c_i32, c_i64, vp, c_i32, vp, c_i64, vp]
     lib.zl_varlen_attn_bwd_workspace_size.restype = c_i32

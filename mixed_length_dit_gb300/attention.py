@@ -79,6 +79,23 @@ def fwd_schedule(cu_seqlens_q, cu_seqlens_k, num_heads, head_dim, tiles=None, dt
     return [tuple(getattr(arr[i], f) for f, _ in _lib.WorkItem._fields_) for i in range(n.value)]
 
 
+def bwd_schedule(cu_seqlens_q, cu_seqlens_k, num_heads, head_dim, tiles=None):
+    """The backward's work items in launch order (host only): a list of
+    (launch, seq, head, k_start, k_len, q_len) tuples
+    (zl_varlen_attn_bwd_schedule)."""
+    lib = _lib.load()
+    cq, nq = _lib.int32_array(cu_seqlens_q)
+    ck, _ = _lib.int32_array(cu_seqlens_k)
+    ta, nt = _lib.tile_array(tiles)
+    n = ctypes.c_int64(0)
+    _lib.check(lib.zl_varlen_attn_bwd_schedule(cq, ck, nq - 1, num_heads, head_dim, ta, nt, None, 0,
+                                               ctypes.byref(n)), "zl_varlen_attn_bwd_schedule")
+    arr = (_lib.BwdWorkItem * max(1, n.value))()
+    _lib.check(lib.zl_varlen_attn_bwd_schedule(cq, ck, nq - 1, num_heads, head_dim, ta, nt, arr, n.value,
+                                               ctypes.byref(n)), "zl_varlen_attn_bwd_schedule")
+    return [tuple(getattr(arr[i], f) for f, _ in _lib.BwdWorkItem._fields_) for i in range(n.value)]
+
+
 def alloc_workspace(nbytes: int, device) -> torch.Tensor | None:
     if nbytes == 0:
         return None

@@ -400,6 +400,28 @@ std::vector<Segment> schedule_fwd(const Plan& p, const int32_t* cu_q, const int3
 }
 
 // Fills args.segs with segments [first, last) and numbers their items.
+// Backward segments.  The backward of a split sequence is the sum over its
+// tiles, which is the backward of the whole sequence: every sequence runs
+// whole, costed by the query rows each of its key blocks visits, stably
+// longest first.
+struct BSeg {
+  zl::BwdSeg seg;
+  int64_t cost;
+  int32_t seq;
+};
+
+std::vector<BSeg> schedule_bwd(const int32_t* cu_q, const int32_t* cu_k, int32_t b) {
+  std::vector<BSeg> segs;
+  for (int32_t i = 0; i < b; ++i) {
+    const int32_t lq = cu_q[i + 1] - cu_q[i];
+    const int32_t lk = cu_k[i + 1] - cu_k[i];
+    if (lq == 0 || lk == 0) continue;
+    segs.push_back(BSeg{zl::BwdSeg{cu_q[i], cu_k[i], lq, lk, 0}, lq, i});
+  }
+  std::stable_sort(segs.begin(), segs.end(), [](const BSeg& a, const BSeg& c) { return a.cost > c.cost; });
+  return segs;
+}
+
 void fill_args(FwdArgs* args, const std::vector<Segment>& segs, size_t first, size_t last, int rows_per_item) {
   int64_t items = 0;
   args->n_segs = static_cast<int32_t>(last - first);
@@ -653,6 +675,40 @@ zl_status zl_varlen_attn_bwd_workspace_size(const int32_t* cu_seqlens_q, const i
   return ZL_OK;
 }
 
+zl_status zl_varlen_attn_bwd_schedule(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs,
+                                      int32_t num_heads, int32_t head_dim, const zl_tile_t* tiles, int32_t num_tiles,
+                                      zl_bwd_work_item_t* items, int64_t max_items, int64_t* n_items) {
+  if (!n_items || max_items < 0 || (max_items > 0 && !items)) return ZL_EINVAL;
+  Plan plan;
+  const zl_status st = make_plan(cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, tiles, num_tiles, &plan);
+  if (st != ZL_OK) return st;
+  const std::vector<BSeg> segs = schedule_bwd(cu_seqlens_q, cu_seqlens_k, num_seqs);
+  // the kernels' numbering: launch by launch, segment by segment, head-major,
+  // key block fastest
+  int64_t n = 0;
+  int32_t launch = 0;
+  for (size_t first = 0; first < segs.size(); first += kMaxSegs, ++launch) {
+    const size_t last = std::min(segs.size(), first + kMaxSegs);
+    for (size_t i = first; i < last; ++i) {
+      const zl::BwdSeg& s = segs[i].seg;
+      const int32_t nkb = (s.k_len + kBlockN - 1) / kBlockN;
+      for (int32_t h = 0; h < num_heads; ++h)
+        for (int32_t kb = 0; kb < nkb; ++kb, ++n) {
+          if (n >= max_items) continue;
+          zl_bwd_work_item_t& w = items[n];
+          w.launch = launch;
+          w.seq = segs[i].seq;
+          w.head = h;
+          w.k_start = kb * kBlockN;
+          w.k_len = std::min(kBlockN, s.k_len - kb * kBlockN);
+          w.q_len = s.q_len;
+        }
+    }
+  }
+  *n_items = n;
+  return ZL_OK;
+}
+
 zl_status zl_varlen_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                              const void* dout, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
                              int32_t num_seqs, int32_t num_heads, int32_t head_dim, int32_t dtype,
@@ -699,21 +755,7 @@ zl_status zl_varlen_attn_bwd(const void* q, const void* k, const void* v, const 
   });
   if (st != ZL_OK) return st;
 
-  // The backward of a split sequence is the sum over its tiles, which is the
-  // backward of the whole sequence: every sequence runs whole here, costed by
-  // the query blocks each of its key blocks visits, longest first.
-  struct BSeg {
-    zl::BwdSeg seg;
-    int64_t cost;
-  };
-  std::vector<BSeg> segs;
-  for (int32_t i = 0; i < num_seqs; ++i) {
-    const int32_t lq = cu_seqlens_q[i + 1] - cu_seqlens_q[i];
-    const int32_t lk = cu_seqlens_k[i + 1] - cu_seqlens_k[i];
-    if (lq == 0 || lk == 0) continue;
-    segs.push_back(BSeg{zl::BwdSeg{cu_seqlens_q[i], cu_seqlens_k[i], lq, lk, 0}, lq});
-  }
-  std::stable_sort(segs.begin(), segs.end(), [](const BSeg& a, const BSeg& c) { return a.cost > c.cost; });
+  const std::vector<BSeg> segs = schedule_bwd(cu_seqlens_q, cu_seqlens_k, num_seqs);
   CUtensorMap mq, mk, mv, mdo, mdq;
   const int bq = zl::bwd_query_block();
   if (!make_map(&mq, q, plan.tq, num_heads, head_dim, bq) || !make_map(&mk, k, plan.tk, num_heads, head_dim) ||

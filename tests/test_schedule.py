@@ -1,8 +1,9 @@
-"""The forward's tile scheduler (host logic, no GPU): work items come in a
+"""The tile schedulers (host logic, no GPU).  Forward: work items come in a
 stable longest-first order of their segments (Zellige §IV-D orders the
 coalesced call's segments stably; §IV-C fills in decreasing price), and
 together they cover every (head, query row, key) of every sequence exactly
-once, within each tile's ranges."""
+once, within each tile's ranges.  Backward: every sequence runs whole, stably
+longest-first by query count, one item per (head, 128-key block)."""
 import collections
 
 import pytest
@@ -131,3 +132,49 @@ def test_schedule_rejects_what_the_forward_rejects():
         zl.fwd_schedule([0, 5], [0, 5], 2, 96)          # unsupported head dim
     with pytest.raises(zl.ZlError):                      # an incomplete tile grid
         zl.fwd_schedule([0, 256], [0, 256], 2, 64, tiles=synth.grid_tiles(0, 256, 256, 2, 2)[:3])
+
+
+def _check_bwd(wl, items, cu_q=None, cu_k=None):
+    cu_q = cu_q or wl.cu_seqlens()
+    cu_k = cu_k or wl.cu_seqlens()
+    H = wl.num_heads
+    # sequences stably longest-first by query count, each head-major, key block fastest
+    order = []
+    for it in items:
+        if not order or order[-1] != (it[0], it[1]):
+            order.append((it[0], it[1]))
+    assert len(order) == len(set(order))
+    lq = [cu_q[s + 1] - cu_q[s] for s in range(len(cu_q) - 1)]
+    assert [(l, -lq[s], s) for l, s in order] == sorted((l, -lq[s], s) for l, s in order)
+    covered = collections.Counter()
+    for _, s, h, k0, kl, ql in items:
+        lk = cu_k[s + 1] - cu_k[s]
+        assert ql == lq[s] and 0 < kl <= 128 and k0 % 128 == 0 and k0 + kl <= lk and 0 <= h < H
+        covered[(s, h)] += kl
+    for s in range(len(cu_q) - 1):
+        lk = cu_k[s + 1] - cu_k[s]
+        want = lk if lq[s] > 0 else 0
+        for h in range(H):
+            assert covered.get((s, h), 0) == want, (s, h)
+    assert max(collections.Counter((i[1], i[2], i[3]) for i in items).values()) == 1
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 7, 8])
+def test_backward_schedule_of_each_workload(n):
+    """Every key block of every head of every sequence once; tiles change
+    nothing (the backward runs every sequence whole)."""
+    wl = synth.config(n)
+    cu = wl.cu_seqlens()
+    items = zl.bwd_schedule(cu, cu, wl.num_heads, wl.head_dim, tiles=wl.tiles() or None)
+    _check_bwd(wl, items)
+    assert items == zl.bwd_schedule(cu, cu, wl.num_heads, wl.head_dim)
+
+
+def test_backward_schedule_ragged_and_keys_without_queries():
+    cu_q = [0, 70, 70, 400, 400]
+    cu_k = [0, 200, 330, 500, 501]
+    wl = synth.Workload("bwd_cross", [70, 0, 330, 0], 2, 128)
+    items = zl.bwd_schedule(cu_q, cu_k, 2, 128)
+    _check_bwd(wl, items, cu_q=cu_q, cu_k=cu_k)
+    assert [s for _, s in dict.fromkeys((i[0], i[1]) for i in items)] == [2, 0]
+    assert len(items) == 2 * (2 + 2)          # sequence 0: 200 keys, sequence 2: 170 keys

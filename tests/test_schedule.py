@@ -178,3 +178,19 @@ def test_backward_schedule_ragged_and_keys_without_queries():
     _check_bwd(wl, items, cu_q=cu_q, cu_k=cu_k)
     assert [s for _, s in dict.fromkeys((i[0], i[1]) for i in items)] == [2, 0]
     assert len(items) == 2 * (2 + 2)          # sequence 0: 200 keys, sequence 2: 170 keys
+
+
+def test_more_segments_than_one_launch_holds():
+    """1,500 sequences exceed one launch's segment table (640): the items
+    spread over three launches, each stably longest-first, all covered once;
+    the backward splits the same way."""
+    rng = __import__("numpy").random.default_rng(5)
+    lens = [int(x) for x in rng.integers(1, 700, size=1500)]
+    wl = synth.Workload("many", lens, 2, 64)
+    items = _schedule(wl)
+    _check(wl, None, items, 256)
+    assert sorted({i[0] for i in items}) == [0, 1, 2]
+    cu = wl.cu_seqlens()
+    bitems = zl.bwd_schedule(cu, cu, 2, 64)
+    _check_bwd(wl, bitems)
+    assert sorted({i[0] for i in bitems}) == [0, 1, 2]

@@ -280,3 +280,25 @@ def test_fig2_mix_dense():
         so = inp["do"][x:y].double().sum(dim=0)
         e = ((sv - so).norm() / so.norm()).item()
         assert e <= 1e-3, (s, e)
+
+
+def test_more_sequences_than_one_launch_holds():
+    """1,400 short sequences (more than two launches' 640-segment tables): the
+    forward and the backward each run as three launches, whose work items
+    are numbered per launch and stolen within their own grid; every output
+    and gradient element against the oracle."""
+    rng = np.random.default_rng(6)
+    lens = [int(x) for x in rng.integers(1, 150, size=1400)]
+    wl = synth.Workload("many", lens, 2, 64)
+    inp = synth.make_inputs(wl, seed=6, device="cuda")
+    cu = wl.cu_seqlens()
+    n0 = zl.launch_count()
+    o, lse = zl.varlen_attn_fwd(inp["q"], inp["k"], inp["v"], cu, cu)
+    zl.sync_check()
+    assert zl.launch_count() - n0 == 3
+    o_ref, l_ref = oracle.varlen_attn_fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), cu, cu)
+    assert np.abs(f64(o) - o_ref).max() <= 2e-2
+    assert np.abs(f64(lse) - l_ref).max() <= 1e-3
+    grads = zl.varlen_attn_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], cu, cu)
+    zl.sync_check()
+    _full_grad_check(inp["q"], inp["k"], inp["v"], inp["do"], cu, cu, grads)

@@ -30,11 +30,12 @@
 // (issued earlier by the same thread, and MMAs of one thread execute in
 // order), and dP^T of block g+1 reuses DP once the softmax-grad warps have
 // loaded dP^T of block g.
-// Each query block's MMAs come from three issuing threads in different warps
-// (one thread issues a tcgen05.mma only every ~70-95 cycles, and the N = 64
-// MMAs here take 32-64 cycles of tensor time each): A issues S^T and dV,
-// B issues dP^T and dK, C issues dQ^T.  A and B issue the S^T / dP^T of the
-// next block before the accumulation of the current one.
+// Each query block's MMAs come from three issuing threads in different warps,
+// one per chain of dependencies (S^T -> dV, dP^T -> dK, dS -> dQ^T), so each
+// product goes out as soon as its own inputs are ready (M128 x N64 MMAs
+// take ~54 cycles each of the shared tensor pipe, N = 128 ones 64): A issues
+// S^T and dV, B issues dP^T and dK, C issues dQ^T.  A and B issue the
+// S^T / dP^T of the next block before the accumulation of the current one.
 //
 // Roles (512 threads, one CTA per SM): warps 0-7 softmax-grad (warp w reads
 // TMEM lanes 32*(w%4).. and query columns 32*(w/4)..) and the dV/dK epilogue,

@@ -7,7 +7,7 @@
 // shards alongside them).  Items arrive ordered longest-first from the host
 // scheduler.  The grid holds one CTA per item, of which one per SM is
 // resident; a resident CTA takes its own item first and then steals the
-// lowest unstarted one from the launch queue (cluster launch control), so an
+// next unstarted one from the launch queue (cluster launch control), so an
 // SM that finishes early picks up the next item in longest-first order.
 //
 // The two query tiles of an item share every K_j / V_j tile that the producer
@@ -20,7 +20,8 @@
 //               S_t = Q_t K_j^T (SS, M=128 N=128) into TMEM, then
 //               O_t += P_t V_j (TS: P read from TMEM, V from shared memory as
 //               an MN-major operand) into TMEM.  One issuing thread per tile,
-//               because a thread issues a tcgen05.mma only every ~70-95 cycles.
+//               so each tile's MMAs go out as soon as its own softmax hands
+//               over, whatever the other tile is doing.
 //   warps 0-7   softmax, warpgroup t for tile t: thread r of the group owns
 //               query row r = TMEM lane r.  Loads its S row, tracks the
 //               running max m and sum l in base 2, writes
@@ -35,8 +36,9 @@
 // TMEM: tile t uses S/P in columns [256t, 256t+128) and O in
 // [256t+128, 256t+128+d); 512 columns.
 //
-// Whole sequences write O in bf16 and LSE in natural log.  Tiles write float32
-// partial O and their own LSE into a partial slot for the merge kernel; with
+// Whole sequences write O in bf16 and LSE in natural log.  Tiles write their
+// partial O (float32, or bf16 when args.part_bf16) and their own LSE into a
+// partial slot for the merge kernel; with
 // the fused merge they then count themselves in an arrival counter per
 // (query block, head) of their query chunk, and the warpgroup that brings the
 // count to the number of kv chunks merges all partials of those 128 rows into

@@ -105,7 +105,9 @@ typedef struct {
 /* Human-readable name of a status code (static string, never NULL). */
 const char* zl_status_string(int32_t status);
 
-/* ABI version of this header: (major << 16) | minor. */
+/* ABI version of this header: (major << 16) | minor.  2.0: head-sharded
+ * tiles; 2.1 adds ZL_FWD_BF16_PARTIALS, zl_lse_merge_ex and the schedule
+ * queries (no existing entry changed). */
 int32_t zl_version(void);
 
 /*

@@ -464,7 +464,7 @@ const char* zl_status_string(int32_t status) {
   }
 }
 
-int32_t zl_version(void) { return (2 << 16) | 0; }
+int32_t zl_version(void) { return (2 << 16) | 1; }
 
 int64_t zl_launch_count(void) { return g_launches.load(); }
 

@@ -215,6 +215,7 @@ extern "C" zl_status zl_varlen_attn_bwd_static(
       items += int64_t(num_heads) * ((args.segs[i].k_len + zl::kBlockN - 1) / zl::kBlockN);
     }
     args.n_segs = n;
+    if (items > INT32_MAX) return ZL_EINVAL;      // more items than a grid (and an int32 index) can hold
     args.n_items = static_cast<int32_t>(items);
     if (zl::launch_bwd_tc(head_dim, mq, mk, mv, mdo, mdq, args, s) != cudaSuccess) {
       cudaGetLastError();

@@ -217,6 +217,7 @@ zl_status make_plan(const int32_t* cu_q, const int32_t* cu_k, int32_t b, int32_t
   st = check_cu(cu_k, b, &plan->tk);
   if (st != ZL_OK) return st;
   if ((plan->tq + kBlockM) * int64_t(nh) * hd > (int64_t(1) << 40)) return ZL_EINVAL;
+  if ((plan->tk + kBlockN) * int64_t(nh) * hd > (int64_t(1) << 40)) return ZL_EINVAL;
   for (int32_t s = 0; s < b; ++s)
     if (cu_q[s + 1] > cu_q[s] && cu_k[s + 1] == cu_k[s]) return ZL_EINVAL;  // queries without keys
   plan->split_index.assign(static_cast<size_t>(b), -1);
@@ -399,7 +400,6 @@ std::vector<Segment> schedule_fwd(const Plan& p, const int32_t* cu_q, const int3
   return segs;
 }
 
-// Fills args.segs with segments [first, last) and numbers their items.
 // Backward segments.  The backward of a split sequence is the sum over its
 // tiles, which is the backward of the whole sequence: every sequence runs
 // whole, costed by the query rows each of its key blocks visits, stably
@@ -422,7 +422,9 @@ std::vector<BSeg> schedule_bwd(const int32_t* cu_q, const int32_t* cu_k, int32_t
   return segs;
 }
 
-void fill_args(FwdArgs* args, const std::vector<Segment>& segs, size_t first, size_t last, int rows_per_item) {
+// Fills args.segs with segments [first, last) and numbers their items; false
+// if the launch would hold more items than a grid (and an int32 index) can.
+bool fill_args(FwdArgs* args, const std::vector<Segment>& segs, size_t first, size_t last, int rows_per_item) {
   int64_t items = 0;
   args->n_segs = static_cast<int32_t>(last - first);
   args->rows_per_item = rows_per_item;
@@ -431,8 +433,10 @@ void fill_args(FwdArgs* args, const std::vector<Segment>& segs, size_t first, si
     s.item0 = static_cast<int32_t>(items);
     args->segs[i - first] = s;
     items += int64_t(s.nh) * ((s.q_len + rows_per_item - 1) / rows_per_item);
+    if (items > INT32_MAX) return false;
   }
   args->n_items = static_cast<int32_t>(items);
+  return true;
 }
 
 zl_status cuda_status(cudaError_t e) {
@@ -626,7 +630,7 @@ zl_status zl_varlen_attn_fwd_ex(const void* q, const void* k, const void* v, con
   }
   for (size_t first = 0; first < segs.size(); first += kMaxSegs) {
     const size_t last = std::min(segs.size(), first + kMaxSegs);
-    fill_args(&args, segs, first, last, dtype == ZL_BF16 ? zl::kFwdRowsPerItem : kBlockM);
+    if (!fill_args(&args, segs, first, last, dtype == ZL_BF16 ? zl::kFwdRowsPerItem : kBlockM)) return ZL_EINVAL;
     if (args.n_items == 0) continue;
     if (dtype == ZL_BF16) {
       st = launch_counted("fwd_tc", s, [&] { return zl::launch_fwd_tc(head_dim, mq, mk, mv, args, s); });
@@ -783,6 +787,7 @@ zl_status zl_varlen_attn_bwd(const void* q, const void* k, const void* v, const 
       args.segs[i - first] = b;
       items += int64_t(num_heads) * ((b.k_len + kBlockN - 1) / kBlockN);
     }
+    if (items > INT32_MAX) return ZL_EINVAL;      // more items than a grid (and an int32 index) can hold
     args.n_items = static_cast<int32_t>(items);
     if (items == 0) continue;
     st = launch_counted("bwd_tc", s, [&] { return zl::launch_bwd_tc(head_dim, mq, mk, mv, mdo, mdq, args, s); });

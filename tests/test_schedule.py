@@ -194,3 +194,13 @@ def test_more_segments_than_one_launch_holds():
     bitems = zl.bwd_schedule(cu, cu, 2, 64)
     _check_bwd(wl, bitems)
     assert sorted({i[0] for i in bitems}) == [0, 1, 2]
+
+
+def test_key_count_bound():
+    """Keys x heads x head dim is bounded as queries are (2^40 elements): a
+    batch past it is rejected before any work, in both directions."""
+    with pytest.raises(zl.ZlError):
+        zl.fwd_schedule([0, 1], [0, 1 << 30], 2048, 128)
+    with pytest.raises(zl.ZlError):
+        zl.bwd_schedule([0, 1], [0, 1 << 30], 2048, 128)
+    assert len(zl.bwd_schedule([0, 1], [0, 1 << 20], 2, 128)) == 2 * (1 << 20) // 128

@@ -137,26 +137,34 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+            lines = f.readlines()
         os.unlink(self.path)
-        if not rows:
-            return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
-        tc = [float(r[9]) for r in rows if len(r) > 9 and r[9].replace(".", "").isdigit()]
-        mem = [float(r[10]) for r in rows if len(r) > 10 and r[10].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows),
-                "power_w": round(statistics.median(pw), 1) if pw else None,
-                "temp_c": max(tc) if tc else None, "mem_mhz": statistics.median(mem) if mem else None}
+        return parse_clock_samples(lines)
+
+
+def parse_clock_samples(lines):
+    """Summary of `nvidia-smi --query-gpu=<ClockSampler.FIELDS>` CSV lines:
+    median SM clock, the highest max clock, the throttle reasons seen active
+    in any sample, median power and memory clock, peak temperature."""
+    rows = []
+    for line in lines:
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) >= 9:
+            rows.append(parts)
+    if not rows:
+        return None
+
+    def column(i):
+        return [float(r[i]) for r in rows if len(r) > i and r[i].replace(".", "").isdigit()]
+
+    sm, mx, pw, tc, mem = column(1), column(2), column(3), column(9), column(10)
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+            "reasons": reasons, "samples": len(rows),
+            "power_w": round(statistics.median(pw), 1) if pw else None,
+            "temp_c": max(tc) if tc else None, "mem_mhz": statistics.median(mem) if mem else None}
 
 
 def gpu_index_for_smi(local_rank: int) -> str:

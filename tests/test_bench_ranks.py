@@ -97,3 +97,38 @@ def test_workload_descriptions_cover_every_workload():
         for s, sp in wl.splits.items():
             assert f"as {'x'.join(str(c) for c in sp)} tiles" in desc
         assert bench.merge_bytes(wl) >= 0
+
+
+def test_clock_samples_summary():
+    """The clock record: median SM clock, every throttle reason seen active
+    in any sample (a hw or thermal slowdown rejects a run), medians of power
+    and memory clock, peak temperature."""
+    lines = [
+        "0, 1980, 2070, 1360.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active, 55, 3996\n",
+        "0, 1965, 2070, 1371.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active, 58, 3996\n",
+        "0, 2010, 2070, 1300.0, 0x0000000000000008, Active, Not Active, Not Active, Not Active, 57, 3996\n",
+        "garbage line\n",
+    ]
+    c = bench.parse_clock_samples(lines)
+    assert c["sm_mhz"] == 1980 and c["sm_max_mhz"] == 2070 and c["samples"] == 3
+    assert c["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert c["power_w"] == 1360.5 and c["temp_c"] == 58 and c["mem_mhz"] == 3996
+    assert bench.parse_clock_samples([]) is None
+    # the older nine-column form still parses
+    c9 = bench.parse_clock_samples(["0, 1900, 2070, 1200, 0x0, Not Active, Not Active, Not Active, Not Active\n"])
+    assert c9["reasons"] == [] and c9["temp_c"] is None
+
+
+def test_traffic_record_follows_the_kernel_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from the record whose source hash matches the
+    kernel source; a record taken on another version reads None."""
+    h = bench.source_hash("bwd_tc.cu")
+    f = tmp_path / "traffic.txt"
+    f.write_text("# comment\n"
+                 f"kernel=bwd_tc workload=train_step src={h} bytes_per_launch=123\n"
+                 "kernel=fwd_tc workload=train_step src=0000000000000000 bytes_per_launch=456\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.recorded_traffic("bwd_tc", "train_step") == 123.0
+    assert bench.recorded_traffic("bwd_tc", "image_mix") is None
+    assert bench.recorded_traffic("fwd_tc", "train_step") is None
+    assert bench.recorded_traffic("nonsense", "train_step") is None

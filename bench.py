@@ -118,10 +118,10 @@ class ClockSampler:
               "temperature.gpu,clocks.mem")
 
     def __init__(self, gpu_index: str):
-        self.path = tempfile.mktemp(prefix="zl_clocks_", suffix=".csv")
+        fd, self.path = tempfile.mkstemp(prefix="zl_clocks_", suffix=".csv")
         self.proc = None
+        self.fh = os.fdopen(fd, "w")
         try:
-            self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
                  "-i", gpu_index], stdout=self.fh, stderr=subprocess.DEVNULL)
@@ -129,18 +129,21 @@ class ClockSampler:
             self.proc = None
 
     def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
+        """Ends sampling and removes the sample file; None if nvidia-smi could
+        not be started."""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
         self.fh.close()
-        with open(self.path) as f:
-            lines = f.readlines()
+        lines = []
+        if self.proc is not None:
+            with open(self.path) as f:
+                lines = f.readlines()
         os.unlink(self.path)
-        return parse_clock_samples(lines)
+        return parse_clock_samples(lines) if self.proc is not None else None
 
 
 def parse_clock_samples(lines):

@@ -132,3 +132,16 @@ def test_traffic_record_follows_the_kernel_source(tmp_path, monkeypatch):
     assert bench.recorded_traffic("bwd_tc", "image_mix") is None
     assert bench.recorded_traffic("fwd_tc", "train_step") is None
     assert bench.recorded_traffic("nonsense", "train_step") is None
+
+
+def test_clock_sampler_cleans_up_without_nvidia_smi(monkeypatch):
+    """Where nvidia-smi cannot start, the sampler reports None and leaves no
+    sample file behind."""
+    def no_smi(*a, **k):
+        raise OSError("no nvidia-smi")
+    monkeypatch.setattr(bench.subprocess, "Popen", no_smi)
+    s = bench.ClockSampler("0")
+    path = s.path
+    assert os.path.exists(path)
+    assert s.stop() is None
+    assert not os.path.exists(path)

@@ -13,7 +13,11 @@ profiler for the attention hot path:
   measured with this library's kernels while the GPU is full (many copies of
   the bucket packed into one coalesced call, time divided by the copies), so
   a price is the sequence's marginal cost inside a busy launch;
-* ``predict_ms()``: the additive estimate of a packed batch, sum of prices.
+* ``predict_ms()``: the additive estimate of a packed batch, sum of prices;
+* ``predict_lpt_ms()``: the same prices replayed through the launch's own
+  schedule: every work item, in the order the library runs them, goes to the
+  SM that comes free first (longest first, as the kernels' work stealing
+  does), so a batch of few large items shows its tail.
 
 The measurement uses CUDA events around the library's calls; no arithmetic
 happens here.
@@ -75,6 +79,54 @@ def predict_ms(seqlens, prices: dict, buckets) -> float:
         t, p = min(by_tokens, key=lambda tp: (abs(tp[0] - L), tp[0]))
         total += p * (L / t) ** 2
     return total
+
+
+def _price(L, by_tokens):
+    t, p = min(by_tokens, key=lambda tp: (abs(tp[0] - L), tp[0]))
+    return p * (L / t) ** 2
+
+
+def predict_lpt_ms(seqlens, prices: dict, buckets, num_heads: int, head_dim: int = 128, sms: int = 152,
+                   fwd_share: float = 0.25, mode: str = "fwd+bwd") -> float:
+    """Makespan estimate of one coalesced call (forward then backward launch
+    for mode "fwd+bwd", the forward alone for "fwd").
+
+    A sequence's price is its GPU time while the GPU is full, i.e. its SM time
+    over `sms`; that SM time is spread over the sequence's work items (from
+    the library's own schedule queries) in proportion to their query x key
+    work, and the items of each launch are dealt in schedule order to the SM
+    that comes free first.  With mode "fwd+bwd" the price is split between
+    the two launches by `fwd_share` (the forward's share of the training
+    step's kernel time, ~0.25 measured); with "fwd" it is all forward.  For a
+    batch with many items per SM this equals predict_ms; with few, it adds
+    the tail."""
+    import heapq
+
+    from . import attention as _attn
+    by_tokens = sorted((b.tokens, prices[b.name]) for b in buckets if b.name in prices)
+    if not by_tokens:
+        raise ValueError("no priced bucket")
+    cu = [0]
+    for L in seqlens:
+        cu.append(cu[-1] + max(0, int(L)))
+    price = [_price(L, by_tokens) if L > 0 else 0.0 for L in seqlens]
+
+    def makespan(items, share):
+        # work of every item of a sequence, to split the sequence's SM time
+        work = [0.0] * len(seqlens)
+        for s, w in items:
+            work[s] += w
+        free = [0.0] * sms
+        for s, w in items:
+            t = heapq.heappop(free)
+            heapq.heappush(free, t + share * price[s] * sms * (w / work[s]))
+        return max(free)
+
+    fwd = [(it[1], float(it[5]) * it[7]) for it in _attn.fwd_schedule(cu, cu, num_heads, head_dim)]
+    if mode == "fwd":
+        return makespan(fwd, 1.0)
+    bwd = [(it[1], float(it[4]) * it[5]) for it in _attn.bwd_schedule(cu, cu, num_heads, head_dim)]
+    return makespan(fwd, fwd_share) + makespan(bwd, 1.0 - fwd_share)
 
 
 def _time_call(fn, reps: int, warmup: int = 2) -> float:

@@ -45,3 +45,28 @@ def test_prices_predict_a_mixed_batch():
     measured = profiler.time_batch(mix, num_heads=12)
     predicted = profiler.predict_ms(mix, prices, bks)
     assert abs(predicted - measured) / measured < 0.25, (predicted, measured)
+
+
+def test_lpt_estimate_equals_additive_when_items_fill_the_sms():
+    """Many equal items per SM: the schedule replay gives the sum of prices."""
+    bks = [profiler.Bucket("a", 1024, "image")]
+    prices = {"a": 2.0}
+    seqs = [1024] * (152 * 2)          # 4 forward items per head x 2 heads each, 32 backward per head
+    lpt = profiler.predict_lpt_ms(seqs, prices, bks, num_heads=2, head_dim=128)
+    assert lpt == pytest.approx(profiler.predict_ms(seqs, prices, bks), rel=1e-9)
+    assert profiler.predict_lpt_ms(seqs, prices, bks, 2, 128, mode="fwd") == \
+        pytest.approx(profiler.predict_ms(seqs, prices, bks), rel=1e-9)
+
+
+def test_lpt_estimate_shows_the_tail_of_few_items():
+    """One sequence with fewer items than SMs takes as long as its longest
+    item, not its share of the GPU."""
+    bks = [profiler.Bucket("a", 1024, "image")]
+    prices = {"a": 1.0}
+    one = profiler.predict_lpt_ms([1024], prices, bks, num_heads=1, head_dim=128, mode="fwd")
+    # 4 equal forward items: each holds an SM for 152/4 of the price
+    assert one == pytest.approx(152 / 4)
+    more = profiler.predict_lpt_ms([1024, 256], prices, bks, num_heads=1, head_dim=128, mode="fwd")
+    assert more >= one
+    with pytest.raises(ValueError):
+        profiler.predict_lpt_ms([10], {}, bks, num_heads=1)

@@ -99,6 +99,9 @@ def attention_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float):
 
 
 def default_scale(head_dim: int) -> float:
+    """The softmax scale used when none is given: 1/sqrt(d).  The pages print
+    no scale; this is the usual scaled dot-product attention, and the tiny
+    correctness batch of the workloads states 1/sqrt(64) at head_dim 64."""
     return 1.0 / math.sqrt(head_dim)
 
 

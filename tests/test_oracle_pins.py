@@ -331,11 +331,55 @@ def pin_one_query_row():
         assert np.all(dq[mask, h] == 0) and np.all(dq[:, [x for x in range(3) if x != h]] == 0)
 
 
+def pin_default_scale():
+    """Without an explicit scale every oracle entry divides the scores by
+    sqrt(d): the printed numbers 1/2 at d = 4, 1/8 at d = 64 (the tiny batch's
+    stated 1/sqrt(64)); a length-1 sequence's LSE is then q.k / 8, summed by a
+    plain loop; and each entry called with no scale returns exactly what it
+    returns with scale 1/8 passed explicitly."""
+    assert of.default_scale(4) == 0.5
+    assert of.default_scale(64) == 0.125
+    assert of.default_scale(16) == 0.25
+    assert abs(of.default_scale(128) * of.default_scale(128) * 128 - 1.0) < 1e-15
+    q, k, v, cu = _packed([1, 3, 2], 2, 64, seed=12)
+    do = _rng(13).standard_normal(q.shape)
+    o, lse = oracle.varlen_attn_fwd(q, k, v, cu, cu)
+    for h in range(2):
+        dot = 0.0
+        for i in range(64):
+            dot += float(q[0, h, i]) * float(k[0, h, i])
+        assert abs(lse[h, 0] - dot / 8.0) < 1e-12
+    o8, lse8 = oracle.varlen_attn_fwd(q, k, v, cu, cu, 0.125)
+    assert np.array_equal(o, o8) and np.array_equal(lse, lse8)
+    g = oracle.varlen_attn_bwd(q, k, v, do, cu, cu)
+    g8 = oracle.varlen_attn_bwd(q, k, v, do, cu, cu, 0.125)
+    assert all(np.array_equal(a, b) for a, b in zip(g, g8))
+    tiles = [(1, 0, 3, 0, 2, 0, 0, 2), (1, 0, 3, 2, 1, 0, 1, 2)]
+    for a, b in zip(oracle.tiled_attn_fwd(q, k, v, cu, cu, tiles),
+                    oracle.tiled_attn_fwd(q, k, v, cu, cu, tiles, 0.125)):
+        assert np.array_equal(a, b)
+    for a, b in zip(oracle.tile_partial(q, k, v, cu, cu, tiles[0]),
+                    oracle.tile_partial(q, k, v, cu, cu, tiles[0], 0.125)):
+        assert np.array_equal(a, b)
+    for a, b in zip(oracle.attention_rows(q, k, v, cu, cu, 1, 0, [0, 2]),
+                    oracle.attention_rows(q, k, v, cu, cu, 1, 0, [0, 2], 0.125)):
+        assert np.array_equal(a, b)
+    assert np.array_equal(oracle.dq_rows(q, k, v, do, cu, cu, 2, 1, [1]),
+                          oracle.dq_rows(q, k, v, do, cu, cu, 2, 1, [1], 0.125))
+    for a, b in zip(oracle.dkdv_rows(q, k, v, do, cu, cu, 1, 1, [0, 2]),
+                    oracle.dkdv_rows(q, k, v, do, cu, cu, 1, 1, [0, 2], 0.125)):
+        assert np.array_equal(a, b)
+    for a, b in zip(oracle.grads_one_query_row(q, k, v, do[1, 0], cu, cu, 1, 0, 0),
+                    oracle.grads_one_query_row(q, k, v, do[1, 0], cu, cu, 1, 0, 0, 0.125)):
+        assert np.array_equal(a, b)
+
+
 PINS = [pin_length_one, pin_constant_keys, pin_identical_values,
         pin_two_keys_closed_form, pin_brute_force_tiny, pin_scipy_softmax,
         pin_merge_equals_unsplit, pin_head_sharded_configurations, pin_merge_empty_parts,
         pin_finite_differences,
-        pin_gradient_sums, pin_sequence_isolation_and_order, pin_row_helpers, pin_one_query_row]
+        pin_gradient_sums, pin_sequence_isolation_and_order, pin_row_helpers, pin_one_query_row,
+        pin_default_scale]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -506,6 +550,14 @@ def _mut_one_row_no_d(q, k, v, do_row, cu_q, cu_k, seq, head, row, scale=None):
     return scale * (ds @ kk)[0], scale * (ds.T @ qr), p.T @ dor
 
 
+def _mut_default_scale_inverse_d(head_dim):
+    return 1.0 / head_dim
+
+
+def _mut_default_scale_sqrt(head_dim):
+    return math.sqrt(head_dim)
+
+
 _REAL = {name: getattr(of, name) for name in
          ("scores", "row_logsumexp", "probabilities", "lse_merge", "grad_scores",
           "grad_q", "grad_k", "grad_v", "tile_heads", "grads_one_query_row")}
@@ -520,6 +572,7 @@ MUTATIONS = [
     ("grad_q", _mut_grad_q_no_scale), ("grad_k", _mut_grad_k_no_transpose),
     ("grad_v", _mut_grad_v_wrong_side), ("tile_heads", _mut_tile_heads_from_zero),
     ("grads_one_query_row", _mut_one_row_no_d),
+    ("default_scale", _mut_default_scale_inverse_d), ("default_scale", _mut_default_scale_sqrt),
 ]
 
 

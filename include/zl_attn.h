@@ -22,8 +22,13 @@
  *   - cu_seqlens_* and tile tables are HOST arrays (int32, num_seqs + 1
  *     entries, cu[0] = 0, non-decreasing).  All other pointers are DEVICE
  *     pointers of the current CUDA device, 16-byte aligned.
- *   - The caller owns every buffer.  The library allocates no device or host
- *     memory; scratch comes from the caller's `workspace`.
+ *   - The caller owns every buffer.  The library never calls cudaMalloc and
+ *     allocates no device memory per call: scratch comes from the caller's
+ *     `workspace` (zl_varlen_attn_bwd_static alone uses a fixed 64 MiB
+ *     array in the library's device image instead, reserved on each device
+ *     the library is loaded on).  On the host, calls build small std::vector
+ *     tables (the schedule, the tile grid) and, while zl_profile_begin is
+ *     active, create two CUDA events per launch.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and return after enqueue.  Arguments are validated on the host
  *     before anything is enqueued; an invalid call returns an error and leaves
@@ -344,7 +349,11 @@ zl_status zl_varlen_attn_bwd(
  * All calls on a device share the array: calls whose kernels may overlap on
  * the GPU (unordered streams) race on it and give undefined results; calls on
  * one stream are safe.  Each call clears the accumulator it uses, so results
- * do not depend on earlier calls.  Allocates no memory.
+ * do not depend on earlier calls.  Allocates no device memory and creates
+ * no CUDA objects: its launches count in zl_launch_count but are not timed
+ * by zl_profile_*, whose events it would have to create.  Batch rules and errors are
+ * zl_varlen_attn_bwd's (token bounds included), checked before the scratch
+ * limit.
  */
 zl_status zl_varlen_attn_bwd_static(
     const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -360,6 +369,20 @@ zl_status zl_varlen_attn_bwd_static(
  * undefined), ZL_ECUDA for a CUDA error.  ZL_OK otherwise.
  */
 zl_status zl_sync_check(void* stream);
+
+/*
+ * Self-test of failure detection.  The pages have no counterpart; what it
+ * exercises is the rule every kernel here follows: no wait is unbounded, a
+ * wait that runs out records an error and ends the CTA's other roles, and the
+ * kernel returns so that the context stays usable.  It enqueues one small
+ * kernel whose wait on an mbarrier that nothing arrives on gives up after
+ * limit_ns nanoseconds (1 .. 1e9; else ZL_EINVAL), while a second warp of
+ * the same CTA, waiting with the kernels' own limit, must leave as soon as the
+ * first one has given up.  No copy or MMA is in flight and no memory is
+ * touched.  The next zl_sync_check(stream) returns ZL_ETIMEOUT (and clears
+ * the record); work enqueued afterwards runs normally.
+ */
+zl_status zl_selftest_wait_timeout(uint64_t limit_ns, void* stream);
 
 /* Number of kernel launches this library has enqueued in this process. */
 int64_t zl_launch_count(void);

@@ -15,10 +15,15 @@
 // on it; calls on one stream, or otherwise ordered, are safe.  The preprocess
 // kernel rewrites all of D and zeroes the part of the accumulator a call uses,
 // so nothing left by an earlier call leaks into the next.
+//
+// Its launches are counted (zl_launch_count) but not timed by the profiling
+// hook: bracketing them would create CUDA events, and this entry point
+// allocates nothing at all.
 #include <algorithm>
 #include <cmath>
 #include <mutex>
 
+#include "host.h"
 #include "launch.h"
 #include "zl_attn.h"
 
@@ -35,11 +40,6 @@ struct StaticDevice {
   zl_status status = ZL_OK;
 };
 StaticDevice g_static_dev[128];
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 // Once per device, with that device current: check it, and look up the device
 // address of the scratch array (in host code the array's name is only a
@@ -81,66 +81,18 @@ zl_status static_setup(float** scratch, int* sms) {
   return d.status;
 }
 
-EncodeTiledFn static_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-    cudaGetLastError();
-  });
-  return fn;
-}
-
-bool static_map(CUtensorMap* map, const void* base, int64_t rows, int nh, int hd, int box_rows = 128) {
-  EncodeTiledFn fn = static_encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nh) * hd, static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nh) * hd * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// float32 view [rows][H*d] of the dQ accumulator: boxes of 32 columns x
-// box_rows rows with the 128-byte swizzle, the shape the backward adds with TMA.
-bool static_map_acc(CUtensorMap* map, const float* base, int64_t rows, int nh, int hd, int box_rows) {
-  EncodeTiledFn fn = static_encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nh) * hd, static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nh) * hd * 4};
-  const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" zl_status zl_varlen_attn_bwd_static(
     const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t num_seqs, int32_t num_heads,
     int32_t head_dim, float softmax_scale, void* dq, void* dk, void* dv, void* stream) {
-  // ---- host-side checks, before any CUDA call
-  if (num_seqs < 0 || num_heads < 1 || num_heads > 4096 || !cu_seqlens_q || !cu_seqlens_k) return ZL_EINVAL;
-  if (head_dim != 64 && head_dim != 128) return ZL_EUNSUPPORTED;
+  // ---- host-side checks, before any CUDA call: the batch rules of every
+  // entry point (token bounds included), then the scratch limit
+  int64_t tq = 0, tk = 0;
+  const zl_status bst = zl::check_batch(cu_seqlens_q, cu_seqlens_k, num_seqs, num_heads, head_dim, &tq, &tk);
+  if (bst != ZL_OK) return bst;
   if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return ZL_EINVAL;
-  if (cu_seqlens_q[0] != 0 || cu_seqlens_k[0] != 0) return ZL_EINVAL;
-  for (int32_t s = 0; s < num_seqs; ++s) {
-    if (cu_seqlens_q[s + 1] < cu_seqlens_q[s] || cu_seqlens_k[s + 1] < cu_seqlens_k[s]) return ZL_EINVAL;
-    if (cu_seqlens_q[s + 1] > cu_seqlens_q[s] && cu_seqlens_k[s + 1] == cu_seqlens_k[s]) return ZL_EINVAL;
-  }
-  const int64_t tq = cu_seqlens_q[num_seqs];
-  const int64_t tk = cu_seqlens_k[num_seqs];
   if (tq == 0 && tk == 0) return ZL_OK;
   // scratch: dQ accumulator [Tq][H][d], then D [H][Tq] at a 256-byte boundary
   const size_t acc_floats = (static_cast<size_t>(tq) * num_heads * head_dim + 63) & ~size_t(63);
@@ -149,7 +101,7 @@ extern "C" zl_status zl_varlen_attn_bwd_static(
   if ((tq > 0 && (!q || !o || !lse || !dout || !dq)) || (tk > 0 && (!k || !v || !dk || !dv))) return ZL_EINVAL;
   const void* ptrs[] = {q, k, v, o, dout, dq, dk, dv, lse};
   for (const void* p : ptrs)
-    if (p && !aligned16(p)) return ZL_EALIGN;
+    if (p && !zl::aligned16(p)) return ZL_EALIGN;
 
   float* scratch = nullptr;
   int sms = 0;
@@ -180,9 +132,9 @@ extern "C" zl_status zl_varlen_attn_bwd_static(
   zl::note_launch();
   CUtensorMap mq, mk, mv, mdo, mdq;
   const int bq = zl::bwd_query_block();
-  if (!static_map(&mq, q, tq, num_heads, head_dim, bq) || !static_map(&mk, k, tk, num_heads, head_dim) ||
-      !static_map(&mv, v, tk, num_heads, head_dim) || !static_map(&mdo, dout, tq, num_heads, head_dim, bq) ||
-      !static_map_acc(&mdq, dq_acc, tq, num_heads, head_dim, bq))
+  if (!zl::make_map(&mq, q, tq, num_heads, head_dim, bq) || !zl::make_map(&mk, k, tk, num_heads, head_dim) ||
+      !zl::make_map(&mv, v, tk, num_heads, head_dim) || !zl::make_map(&mdo, dout, tq, num_heads, head_dim, bq) ||
+      !zl::make_map_acc(&mdq, dq_acc, tq, num_heads, head_dim, bq))
     return ZL_ECUDA;
   static thread_local zl::BwdArgs args;
   args.lse = lse;

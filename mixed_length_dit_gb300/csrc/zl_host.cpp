@@ -23,6 +23,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "host.h"
 #include "launch.h"
 #include "zl_attn.h"
 
@@ -33,6 +34,10 @@ using zl::FwdSeg;
 using zl::kBlockM;
 using zl::kBlockN;
 using zl::kMaxSegs;
+using zl::aligned16;
+using zl::launch_counted;
+using zl::make_map;
+using zl::make_map_acc;
 
 std::atomic<int64_t> g_launches{0};
 
@@ -45,48 +50,6 @@ struct ProfRecord {
 std::mutex g_prof_mu;
 bool g_prof_on = false;
 std::vector<ProfRecord> g_prof;
-
-// Launches through `fn`, counting it and, while profiling, bracketing it with
-// events on `stream`.
-template <typename F>
-zl_status launch_counted(const char* name, cudaStream_t stream, F fn) {
-  cudaEvent_t a = nullptr, b = nullptr;
-  bool prof = false;
-  {
-    std::lock_guard<std::mutex> lock(g_prof_mu);
-    prof = g_prof_on;
-  }
-  if (prof) {
-    if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess ||
-        cudaEventRecord(a, stream) != cudaSuccess) {
-      cudaGetLastError();
-      if (a) cudaEventDestroy(a);
-      if (b) cudaEventDestroy(b);
-      return ZL_ECUDA;
-    }
-  }
-  const cudaError_t e = fn();
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    if (prof) {
-      cudaEventDestroy(a);
-      cudaEventDestroy(b);
-    }
-    return ZL_ECUDA;
-  }
-  g_launches.fetch_add(1);
-  if (prof) {
-    if (cudaEventRecord(b, stream) != cudaSuccess) {
-      cudaGetLastError();
-      cudaEventDestroy(a);
-      cudaEventDestroy(b);
-      return ZL_ECUDA;
-    }
-    std::lock_guard<std::mutex> lock(g_prof_mu);
-    g_prof.push_back(ProfRecord{name, a, b});
-  }
-  return ZL_OK;
-}
 
 // ------------------------------------------------------------------ device
 struct DevInfo {
@@ -123,56 +86,6 @@ zl_status device_sms(int* sms) {
   return static_cast<zl_status>(d.status);
 }
 
-// ------------------------------------------------------------------ tensor maps
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-    cudaGetLastError();
-  });
-  return fn;
-}
-
-// 2D view [rows][H*d] of a packed bf16 tensor; boxes of 64 columns x 128 rows
-// with the 128-byte swizzle the UMMA descriptors expect.  Rows past the end
-// read as zero.
-bool make_map(CUtensorMap* map, const void* base, int64_t rows, int nh, int hd, int box_rows = 128) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nh) * hd, static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nh) * hd * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// float32 view [rows][H*d] of the dQ accumulator: boxes of 32 columns x
-// box_rows rows with the 128-byte swizzle, the shape the backward adds with TMA.
-bool make_map_acc(CUtensorMap* map, const float* base, int64_t rows, int nh, int hd, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nh) * hd, static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nh) * hd * 4};
-  const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // ------------------------------------------------------------------ validation
 struct SplitSeq {
   int seq = 0;
@@ -194,32 +107,21 @@ struct Plan {
   int64_t n_counters = 0;           // arrival counters: (query chunk, 128-row block) x head
 };
 
-constexpr int64_t kMaxTokens = (int64_t(1) << 31) - 1 - 2 * kBlockM;
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 zl_status check_cu(const int32_t* cu, int32_t b, int64_t* total) {
   if (!cu) return ZL_EINVAL;
   if (cu[0] != 0) return ZL_EINVAL;
   for (int32_t s = 0; s < b; ++s)
     if (cu[s + 1] < cu[s]) return ZL_EINVAL;
   *total = cu[b];
-  if (*total > kMaxTokens) return ZL_EINVAL;
+  if (*total > zl::kMaxTokens) return ZL_EINVAL;
   return ZL_OK;
 }
 
 zl_status make_plan(const int32_t* cu_q, const int32_t* cu_k, int32_t b, int32_t nh, int32_t hd,
                     const zl_tile_t* tiles, int32_t n_tiles, Plan* plan) {
-  if (b < 0 || n_tiles < 0 || nh < 1 || nh > 4096) return ZL_EINVAL;
-  if (hd != 64 && hd != 128) return ZL_EUNSUPPORTED;
-  zl_status st = check_cu(cu_q, b, &plan->tq);
+  if (n_tiles < 0) return ZL_EINVAL;
+  const zl_status st = zl::check_batch(cu_q, cu_k, b, nh, hd, &plan->tq, &plan->tk);
   if (st != ZL_OK) return st;
-  st = check_cu(cu_k, b, &plan->tk);
-  if (st != ZL_OK) return st;
-  if ((plan->tq + kBlockM) * int64_t(nh) * hd > (int64_t(1) << 40)) return ZL_EINVAL;
-  if ((plan->tk + kBlockN) * int64_t(nh) * hd > (int64_t(1) << 40)) return ZL_EINVAL;
-  for (int32_t s = 0; s < b; ++s)
-    if (cu_q[s + 1] > cu_q[s] && cu_k[s + 1] == cu_k[s]) return ZL_EINVAL;  // queries without keys
   plan->split_index.assign(static_cast<size_t>(b), -1);
   plan->splits.clear();
   plan->tiles.clear();
@@ -448,7 +350,108 @@ zl_status cuda_status(cudaError_t e) {
 }  // namespace
 
 namespace zl {
+
 void note_launch() { g_launches.fetch_add(1); }
+
+zl_status check_batch(const int32_t* cu_q, const int32_t* cu_k, int32_t num_seqs, int32_t num_heads,
+                      int32_t head_dim, int64_t* tq, int64_t* tk) {
+  if (num_seqs < 0 || num_heads < 1 || num_heads > 4096) return ZL_EINVAL;
+  if (head_dim != 64 && head_dim != 128) return ZL_EUNSUPPORTED;
+  zl_status st = check_cu(cu_q, num_seqs, tq);
+  if (st != ZL_OK) return st;
+  st = check_cu(cu_k, num_seqs, tk);
+  if (st != ZL_OK) return st;
+  if ((*tq + kBlockM) * int64_t(num_heads) * head_dim > (int64_t(1) << 40)) return ZL_EINVAL;
+  if ((*tk + kBlockN) * int64_t(num_heads) * head_dim > (int64_t(1) << 40)) return ZL_EINVAL;
+  for (int32_t s = 0; s < num_seqs; ++s)
+    if (cu_q[s + 1] > cu_q[s] && cu_k[s + 1] == cu_k[s]) return ZL_EINVAL;  // queries without keys
+  return ZL_OK;
+}
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+}  // namespace
+
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int nh, int hd, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nh) * hd, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nh) * hd * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_acc(CUtensorMap* map, const float* base, int64_t rows, int nh, int hd, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(nh) * hd, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(nh) * hd * 4};
+  const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+zl_status prof_before(ProfScope* p, cudaStream_t stream) {
+  {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    p->on = g_prof_on;
+  }
+  if (!p->on) return ZL_OK;
+  if (cudaEventCreate(&p->start) != cudaSuccess || cudaEventCreate(&p->stop) != cudaSuccess ||
+      cudaEventRecord(p->start, stream) != cudaSuccess) {
+    cudaGetLastError();
+    if (p->start) cudaEventDestroy(p->start);
+    if (p->stop) cudaEventDestroy(p->stop);
+    return ZL_ECUDA;
+  }
+  return ZL_OK;
+}
+
+zl_status prof_after(ProfScope* p, const char* name, cudaStream_t stream, cudaError_t launch_error) {
+  if (launch_error != cudaSuccess) {
+    cudaGetLastError();
+    if (p->on) {
+      cudaEventDestroy(p->start);
+      cudaEventDestroy(p->stop);
+    }
+    return ZL_ECUDA;
+  }
+  g_launches.fetch_add(1);
+  if (!p->on) return ZL_OK;
+  if (cudaEventRecord(p->stop, stream) != cudaSuccess) {
+    cudaGetLastError();
+    cudaEventDestroy(p->start);
+    cudaEventDestroy(p->stop);
+    return ZL_ECUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof.push_back(ProfRecord{name, p->start, p->stop});
+  return ZL_OK;
+}
+
 }  // namespace zl
 
 // =================================================================== C ABI
@@ -849,9 +852,19 @@ zl_status zl_sync_check(void* stream) {
   }
   const uint32_t ef = zl::fwd_take_error();
   const uint32_t eb = zl::bwd_take_error();
-  if (ef == 0xFFFFFFFFu || eb == 0xFFFFFFFFu) return ZL_ECUDA;
-  if (ef != 0 || eb != 0) return ZL_ETIMEOUT;
+  const uint32_t es = zl::selftest_take_error();
+  if (ef == 0xFFFFFFFFu || eb == 0xFFFFFFFFu || es == 0xFFFFFFFFu) return ZL_ECUDA;
+  if (ef != 0 || eb != 0 || es != 0) return ZL_ETIMEOUT;
   return ZL_OK;
+}
+
+zl_status zl_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > 1000000000ull) return ZL_EINVAL;
+  int sms = 0;
+  const zl_status st = device_sms(&sms);
+  if (st != ZL_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return launch_counted("selftest_wait", s, [&] { return zl::launch_wait_timeout_selftest(limit_ns, s); });
 }
 
 }  // extern "C"

@@ -206,6 +206,37 @@ def test_bwd_argument_checks(lib):
     assert lib.zl_varlen_attn_bwd(*args, _lib.ZL_BF16, 0.0, *tail) == _lib.ZL_EINVAL
 
 
+def test_static_bwd_applies_the_batch_bounds(lib):
+    """The workspace-free backward checks a batch as zl_varlen_attn_bwd does,
+    token bounds included, before its scratch limit and before any CUDA call:
+    an oversized key count is an invalid argument, not a scratch overflow."""
+    p = ctypes.c_void_p(64)
+    cq, nq = _lib.int32_array([0, 5])
+    for ck_list, nh in (([0, (1 << 31) - 100], 2),          # more keys than int32 row indices allow
+                        ([0, (1 << 31) - 300], 4096),       # (Tk + block) * H * d > 2^40
+                        ([0, 3000], 8192)):                 # too many heads
+        ck, _ = _lib.int32_array(ck_list)
+        args = [p] * 6 + [cq, ck, 1, nh, 128, 0.125, p, p, p, None]
+        assert lib.zl_varlen_attn_bwd_static(*args) == _lib.ZL_EINVAL, (ck_list, nh)
+        wargs = [p] * 6 + [cq, ck, 1, nh, 128, _lib.ZL_BF16, 0.125, None, 0, p, p, p, p, 1 << 40, None]
+        assert lib.zl_varlen_attn_bwd(*wargs) == _lib.ZL_EINVAL, (ck_list, nh)
+    bad, _ = _lib.int32_array([0, 7, 5])
+    assert lib.zl_varlen_attn_bwd_static(*([p] * 6), bad, bad, 2, 2, 64, 0.125, p, p, p, None) == _lib.ZL_EINVAL
+    assert lib.zl_varlen_attn_bwd_static(*([p] * 6), cq, cq, 1, 2, 96, 0.125, p, p, p, None) == \
+        _lib.ZL_EUNSUPPORTED
+    # past the scratch limit: 131,072 query tokens at 40 heads x 128
+    big, _ = _lib.int32_array([0, 131072])
+    assert lib.zl_varlen_attn_bwd_static(*([p] * 6), big, big, 1, 40, 128, 0.125, p, p, p, None) == \
+        _lib.ZL_EWORKSPACE
+
+
+def test_selftest_limit_is_checked_first(lib):
+    """The wait self-test takes limits of 1 ns .. 1 s only, checked before
+    any CUDA call."""
+    assert lib.zl_selftest_wait_timeout(0, None) == _lib.ZL_EINVAL
+    assert lib.zl_selftest_wait_timeout(1_000_000_001, None) == _lib.ZL_EINVAL
+
+
 def test_no_device_is_reported_not_crashed(lib):
     import torch
     if torch.cuda.is_available():

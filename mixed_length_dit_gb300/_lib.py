@@ -30,6 +30,7 @@ EXPORTS = (
     "zl_lse_merge", "zl_varlen_attn_bwd_workspace_size", "zl_varlen_attn_bwd", "zl_sync_check",
     "zl_launch_count", "zl_profile_begin", "zl_profile_end", "zl_varlen_attn_bwd_static",
     "zl_varlen_attn_fwd_ex", "zl_lse_merge_ex", "zl_varlen_attn_fwd_schedule", "zl_varlen_attn_bwd_schedule",
+    "zl_selftest_wait_timeout",
 )
 
 ZL_FWD_FUSED_MERGE = 1
@@ -89,6 +90,8 @@ def load() -> ctypes.CDLL:
     lib.zl_launch_count.argtypes = []
     lib.zl_sync_check.restype = c_i32
     lib.zl_sync_check.argtypes = [vp]
+    lib.zl_selftest_wait_timeout.restype = c_i32
+    lib.zl_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.zl_varlen_attn_fwd_workspace_size.restype = c_i32
     lib.zl_varlen_attn_fwd_workspace_size.argtypes = [i32p, i32p, c_i32, c_i32, c_i32, tilep, c_i32, szp]
     lib.zl_varlen_attn_fwd.restype = c_i32

@@ -68,10 +68,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits until the phase with the given parity has completed.  Returns false
 // (after recording `code` in *err and raising *abort_flag) if the wait ran
-// past the limit or another role of the CTA already aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag,
-                                          uint32_t* err, uint32_t code) {
+// past `limit_ns`, or returns false at once if another role of the CTA
+// already aborted.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity,
+                                                volatile int* abort_flag,
+                                                uint32_t* err, uint32_t code, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
@@ -79,12 +80,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > ZL_WAIT_LIMIT_NS) {
+    if (globaltimer() - t0 > limit_ns) {
       *abort_flag = 1;
       atomicOr(err, code);
       return false;
     }
   }
+}
+
+// mbar_wait_limit with the kernels' limit, ZL_WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          volatile int* abort_flag,
+                                          uint32_t* err, uint32_t code) {
+  return mbar_wait_limit(bar, parity, abort_flag, err, code, ZL_WAIT_LIMIT_NS);
 }
 
 // ---------------------------------------------------------------- TMA

@@ -131,5 +131,10 @@ size_t bwd_tc_smem_bytes(int head_dim);
 // cleared; synchronous).
 uint32_t fwd_take_error();
 uint32_t bwd_take_error();
+uint32_t selftest_take_error();
+
+// One CTA whose wait on an mbarrier nobody arrives on runs out after
+// limit_ns (the bounded-wait self-test; see zl_selftest_wait_timeout).
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace zl

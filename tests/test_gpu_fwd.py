@@ -59,6 +59,20 @@ def test_tiny_fp32(split):
     _full_check(inp["q"], inp["k"], inp["v"], cu, cu, o, lse, TOL_FP32, TOL_FP32)
 
 
+@pytest.mark.parametrize("split", [False, True])
+def test_tiny_fp32_head_dim_128(split):
+    """The float32 path at head_dim 128, whose kernel splits each query row's
+    dot products over two threads: the tiny batch's lengths at d = 128, whole
+    and with the 256-token sequence as a 2 x 2 tile grid."""
+    wl = synth.Workload("tiny128", [37, 64, 100, 256], 2, 128)
+    inp = synth.make_inputs(wl, seed=3, device="cuda", dtype=torch.float32, with_grad_out=False)
+    tiles = synth.grid_tiles(3, 256, 256, 2, 2) if split else None
+    o, lse = _run(inp, wl, tiles)
+    assert o.dtype == torch.float32
+    cu = wl.cu_seqlens()
+    _full_check(inp["q"], inp["k"], inp["v"], cu, cu, o, lse, TOL_FP32, TOL_FP32)
+
+
 @pytest.mark.parametrize("hd", [64, 128])
 def test_ragged_edges(hd):
     """Lengths around the 128-row block: 1, 2, 127, 128, 129, 255, 257, an

@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload 1..9] [--mode step|fwd] [--seed S] [--bf16-partials]
-                    [--no-e2e] [--no-cpu-baseline]
+                    [--no-e2e] [--no-cpu-baseline] [--per-config 2,3,4 | --per-config none]
 
 One step = one pass of the whole path over one batch: the forward over whole
 sequences and shard tiles in one launch, the exact LSE merge of the tiles, the
@@ -32,6 +32,14 @@ source), the oracle's CPU throughput on a bounded sample, an end-to-end leg
 own clock record, the number of library launches, and the SM clock, power,
 temperature and throttle reasons sampled while each timed region ran.
 --bf16-partials keeps the partial rows of key-split sequences in bf16.
+
+`per_config` adds, for the image-only mix (2), the mixed Wan batch (3) and the
+131,072-token shard mode (4), the forward (with its merge) and the fwd+bwd
+step timed on their own batches: CUDA events over K steps after 3 warm-up
+steps (K chosen so each timed region lasts about half a second, at least 5
+steps), each with its own clock record and its fraction of the burst and
+sustained bf16 peaks, against the target of 60% (forward) and 45% (fwd+bwd)
+of the dense bf16 peak.
 """
 from __future__ import annotations
 
@@ -76,9 +84,39 @@ def source_hash(name: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from an ncu capture (profiles/traffic.txt), or
-    None when missing or taken on a different version of the kernel source."""
+def algorithmic_bytes(wl, kernel: str, bf16_partials: bool = False) -> float:
+    """Algorithmic DRAM bytes of one step's launches of `kernel` (every input
+    read once, every output written once):
+      fwd_tc   q, k, v read; bf16 O and float32 LSE of whole sequences and of
+               sequences split only by queries and heads written; the partial
+               O (float32, or bf16) and LSE of every key chunk of a key-split
+               sequence written;
+      bwd_tc   q, k, v, dO (bf16) and LSE, D (float32) read; dK, dV written;
+               the float32 dQ accumulator read and written once;
+      lse_merge  merge_bytes."""
+    h, d = wl.num_heads, wl.head_dim
+    t = wl.total_tokens
+    if kernel == "lse_merge":
+        return merge_bytes(wl, bf16_partials)
+    if kernel == "bwd_tc":
+        return t * h * (4 * d * 2 + 2 * 4 + 2 * d * 2 + 2 * d * 4)
+    if kernel == "fwd_tc":
+        part = (2 if bf16_partials else 4) * d + 4
+        total = 3.0 * t * h * d * 2
+        for s, n in enumerate(wl.seqlens):
+            n_kv = wl.splits.get(s, (1, 1))[1]
+            total += n * h * (n_kv * part if n_kv > 1 else 2 * d + 4)
+        return total
+    raise KeyError(kernel)
+
+
+def recorded_traffic(kernel: str, wl, bf16_partials: bool = False):
+    """DRAM bytes per step of `kernel` on workload wl, scaled from a capture:
+    profiles/traffic.txt records, per kernel, the DRAM bytes of one launch on
+    a small workload (dram__bytes_read.sum + dram__bytes_write.sum) and that
+    launch's algorithmic bytes; the ratio of the two times wl's algorithmic
+    bytes is the estimate.  None when no record exists for the current kernel
+    source (src hash)."""
     try:
         with open(TRAFFIC_FILE) as f:
             lines = f.read().splitlines()
@@ -92,8 +130,10 @@ def recorded_traffic(kernel: str, workload: str):
         if line.startswith("#") or not line.strip():
             continue
         f = dict(x.split("=", 1) for x in line.split())
-        if f.get("kernel") == kernel and f.get("workload") == workload and f.get("src") == h:
-            return float(f["bytes_per_launch"])
+        if f.get("kernel") == kernel and f.get("src") == h and "algorithmic_bytes" in f:
+            ratio = float(f["bytes_per_launch"]) / float(f["algorithmic_bytes"])
+            return {"bytes": ratio * algorithmic_bytes(wl, kernel, bf16_partials), "ratio": round(ratio, 4),
+                    "captured_on": f.get("workload")}
     return None
 
 
@@ -244,6 +284,67 @@ def cpu_threads() -> int:
     return os.cpu_count() or 1
 
 
+# ----------------------------------------------------------------- per configuration
+TARGET_FRAC = {"fwd": 0.60, "step": 0.45}
+
+
+def time_config(zl, n: int, dev, seed: int, peaks, target_s: float = 0.5, warmup: int = 3):
+    """Forward (with its merge) and fwd+bwd step of workload n, each timed by
+    itself: `warmup` untimed calls (timed as a group to size the run), then K
+    calls bracketed by CUDA events on the launching stream, with the clocks
+    sampled meanwhile.  Returns one dict per mode."""
+    wl = synth.config(n)
+    inp = synth.make_inputs(wl, seed=seed, device=dev)
+    cu = wl.cu_seqlens()
+    tiles = wl.tiles() or None
+    H, D, T = wl.num_heads, wl.head_dim, wl.total_tokens
+    o = torch.empty_like(inp["q"])
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    fws = zl.alloc_workspace(zl.fwd_workspace_bytes(cu, cu, H, D, tiles), dev)
+    dq, dk, dv = (torch.empty_like(inp["q"]) for _ in range(3))
+    bws = zl.alloc_workspace(zl.bwd_workspace_bytes(cu, cu, H, D), dev)
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    out = {"workload": workload_desc(wl)}
+    for mode in ("fwd", "step"):
+        def run():
+            zl.varlen_attn_fwd(inp["q"], inp["k"], inp["v"], cu, cu, tiles=tiles, out=o, lse=lse, workspace=fws)
+            if mode == "step":
+                zl.varlen_attn_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], cu, cu, tiles=tiles,
+                                   dq=dq, dk=dk, dv=dv, workspace=bws)
+        w0 = torch.cuda.Event(enable_timing=True)
+        w1 = torch.cuda.Event(enable_timing=True)
+        w0.record()
+        for _ in range(warmup):
+            run()
+        w1.record()
+        torch.cuda.synchronize()
+        zl.sync_check()
+        est_ms = w0.elapsed_time(w1) / warmup
+        steps = max(5, int(np.ceil(target_s * 1e3 / max(est_ms, 1e-3))))
+        sampler = ClockSampler(gpu_index_for_smi(dev.index or 0))
+        time.sleep(0.3)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        clocks = sampler.stop()
+        zl.sync_check()
+        ms = e0.elapsed_time(e1) / steps
+        flops = fwd_flops(wl) * (3.5 if mode == "step" else 1.0)
+        tf = flops / (ms * 1e-3) / 1e12
+        out[mode] = {"tflops": round(tf, 1), "ms": round(ms, 4), "steps": steps, "flops": flops,
+                     "frac_burst": round(tf / burst, 4), "frac_sustained": round(tf / sustained, 4),
+                     "target_frac_burst": TARGET_FRAC[mode], "meets_target": bool(tf / burst >= TARGET_FRAC[mode]),
+                     "clocks": clocks}
+    del inp, o, lse, fws, dq, dk, dv, bws
+    torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -262,6 +363,9 @@ def main():
                     help="length of the sequence whose heads the CPU oracle times")
     ap.add_argument("--oracle-heads", type=int, default=16,
                     help="number of heads of that sequence the CPU oracle times")
+    ap.add_argument("--per-config", default="2,3,4",
+                    help="workloads whose forward and fwd+bwd step are also timed by themselves "
+                         "(comma-separated; 'none' to skip)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -339,12 +443,16 @@ def main():
     if dom is not None:
         n_l, tot = prof[dom]
         avg_ms = tot / n_l
-        traffic = recorded_traffic(dom, wl.name)
+        rec = recorded_traffic(dom, wl, args.bf16_partials)
+        # per launch, scaled from the small-case capture's ratio to its algorithmic bytes
+        traffic = round(rec["bytes"] * args.steps / n_l) if rec else None
+        traffic_note = (f"ncu DRAM bytes of one launch on {rec['captured_on']} = {rec['ratio']} x its "
+                        f"algorithmic bytes, times this launch's algorithmic bytes") if rec else None
         if dom in ("fwd_tc", "bwd_tc"):
             per_launch = (flops_fwd if dom == "fwd_tc" else 2.5 * flops_fwd) * args.steps / n_l
             ach = per_launch / (avg_ms * 1e-3) / 1e12
             roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": sustained, "unit": "TFLOP/s",
-                    "frac": round(ach / sustained, 4), "traffic": traffic,
+                    "frac": round(ach / sustained, 4), "traffic": traffic, "traffic_note": traffic_note,
                     "kernel": dom, "peak_kind": f"bf16 sustained ({peak_kind})",
                     "flops_per_launch": per_launch, "avg_launch_ms": round(avg_ms, 4)}
         elif dom == "lse_merge":
@@ -352,7 +460,8 @@ def main():
             per_launch = merge_bytes(wl, args.bf16_partials) * args.steps / max(1, n_l)
             ach = per_launch / (avg_ms * 1e-3) / 1e9
             roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
-                    "frac": round(ach / hbm, 4), "traffic": traffic, "kernel": dom}
+                    "frac": round(ach / hbm, 4), "traffic": traffic, "traffic_note": traffic_note,
+                    "kernel": dom}
     kernels = {k: {"launches": v[0], "avg_ms": round(v[1] / v[0], 4),
                    "share": round(v[1] / sum(x[1] for x in prof.values()), 4)} for k, v in prof.items()}
     fwd_ms = sum(prof[k][1] for k in ("fwd_tc", "lse_merge") if k in prof) / args.steps
@@ -439,6 +548,13 @@ def main():
                "clocks": e2e_clocks}
         del dev_in, dev_out, host_in, host_out, lse2
 
+    # ---------------- forward and fwd+bwd per configuration, each timed by itself
+    per_config = None
+    if args.per_config.strip().lower() not in ("", "none"):
+        per_config = {}
+        for n in (int(x) for x in args.per_config.split(",")):
+            per_config[str(n)] = time_config(zl, n, dev, args.seed + rank, peaks)
+
     # ---------------- CPU oracle baseline (rank 0, single GPU)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -481,6 +597,7 @@ def main():
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "per_config": per_config,
         "gpu_launches": launches,
         "clocks": clocks,
     }

@@ -120,18 +120,36 @@ def test_clock_samples_summary():
 
 
 def test_traffic_record_follows_the_kernel_source(tmp_path, monkeypatch):
-    """roofline.traffic comes from the record whose source hash matches the
-    kernel source; a record taken on another version reads None."""
+    """roofline.traffic is scaled from the record whose source hash matches
+    the kernel source (its DRAM bytes over its algorithmic bytes, times the
+    bench workload's algorithmic bytes); a record taken on another version of
+    the source reads None."""
+    import synth
     h = bench.source_hash("bwd_tc.cu")
     f = tmp_path / "traffic.txt"
     f.write_text("# comment\n"
-                 f"kernel=bwd_tc workload=train_step src={h} bytes_per_launch=123\n"
-                 "kernel=fwd_tc workload=train_step src=0000000000000000 bytes_per_launch=456\n")
+                 f"kernel=bwd_tc workload=small src={h} bytes_per_launch=300 algorithmic_bytes=200\n"
+                 "kernel=fwd_tc workload=small src=0000000000000000 bytes_per_launch=456 algorithmic_bytes=400\n")
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
-    assert bench.recorded_traffic("bwd_tc", "train_step") == 123.0
-    assert bench.recorded_traffic("bwd_tc", "image_mix") is None
-    assert bench.recorded_traffic("fwd_tc", "train_step") is None
-    assert bench.recorded_traffic("nonsense", "train_step") is None
+    wl = synth.config(5)
+    rec = bench.recorded_traffic("bwd_tc", wl)
+    assert rec["ratio"] == 1.5 and rec["captured_on"] == "small"
+    assert rec["bytes"] == 1.5 * bench.algorithmic_bytes(wl, "bwd_tc")
+    assert bench.recorded_traffic("fwd_tc", wl) is None
+    assert bench.recorded_traffic("nonsense", wl) is None
+
+
+def test_algorithmic_bytes_of_the_training_step():
+    """The training-step batch's algorithmic bytes per step, from the sizes:
+    T = 190,272 tokens, H = 40, d = 128; the 75,600-token video split 2 x 2."""
+    import synth
+    wl = synth.config(5)
+    thd = 190272 * 40 * 128
+    assert bench.algorithmic_bytes(wl, "bwd_tc") == thd * 2 * 4 + 190272 * 40 * 8 + thd * 2 * 2 + thd * 8
+    whole = (190272 - 75600) * 40 * (2 * 128 + 4)
+    parts = 2 * 75600 * 40 * (4 * 128 + 4)
+    assert bench.algorithmic_bytes(wl, "fwd_tc") == 3 * thd * 2 + whole + parts
+    assert bench.algorithmic_bytes(wl, "lse_merge") == bench.merge_bytes(wl)
 
 
 def test_clock_sampler_cleans_up_without_nvidia_smi(monkeypatch):

@@ -52,10 +52,13 @@ def test_lpt_estimate_equals_additive_when_items_fill_the_sms():
     bks = [profiler.Bucket("a", 1024, "image")]
     prices = {"a": 2.0}
     seqs = [1024] * (152 * 2)          # 4 forward items per head x 2 heads each, 32 backward per head
-    lpt = profiler.predict_lpt_ms(seqs, prices, bks, num_heads=2, head_dim=128)
+    lpt = profiler.predict_lpt_ms(seqs, prices, bks, num_heads=2, head_dim=128, sms=152)
     assert lpt == pytest.approx(profiler.predict_ms(seqs, prices, bks), rel=1e-9)
-    assert profiler.predict_lpt_ms(seqs, prices, bks, 2, 128, mode="fwd") == \
+    assert profiler.predict_lpt_ms(seqs, prices, bks, 2, 128, sms=152, mode="fwd") == \
         pytest.approx(profiler.predict_ms(seqs, prices, bks), rel=1e-9)
+    # a measured forward price splits the sequence's time between the launches
+    lpt_f = profiler.predict_lpt_ms(seqs, prices, bks, 2, 128, sms=152, fwd_prices={"a": 0.5})
+    assert lpt_f == pytest.approx(profiler.predict_ms(seqs, prices, bks), rel=1e-9)
 
 
 def test_lpt_estimate_shows_the_tail_of_few_items():
@@ -63,10 +66,40 @@ def test_lpt_estimate_shows_the_tail_of_few_items():
     item, not its share of the GPU."""
     bks = [profiler.Bucket("a", 1024, "image")]
     prices = {"a": 1.0}
-    one = profiler.predict_lpt_ms([1024], prices, bks, num_heads=1, head_dim=128, mode="fwd")
+    one = profiler.predict_lpt_ms([1024], prices, bks, num_heads=1, head_dim=128, sms=152, mode="fwd")
     # 4 equal forward items: each holds an SM for 152/4 of the price
     assert one == pytest.approx(152 / 4)
-    more = profiler.predict_lpt_ms([1024, 256], prices, bks, num_heads=1, head_dim=128, mode="fwd")
+    more = profiler.predict_lpt_ms([1024, 256], prices, bks, num_heads=1, head_dim=128, sms=152, mode="fwd")
     assert more >= one
     with pytest.raises(ValueError):
-        profiler.predict_lpt_ms([10], {}, bks, num_heads=1)
+        profiler.predict_lpt_ms([10], {}, bks, num_heads=1, sms=152)
+
+
+def test_lpt_estimate_with_a_tile_table():
+    """A split sequence's forward items come from its tiles; its price is the
+    whole sequence's, spread over the tiles' items by their work.  A 2 x 2
+    grid of one 2,048-token sequence on one head: 16 forward items (four
+    query blocks of 256 rows in each of the 4 tiles of 1,024 x 1,024) of
+    equal work."""
+    import synth
+    bks = [profiler.Bucket("a", 2048, "video")]
+    tiles = synth.grid_tiles(0, 2048, 2048, 2, 2)
+    one = profiler.predict_lpt_ms([2048], {"a": 1.0}, bks, num_heads=1, head_dim=128, sms=152, mode="fwd",
+                                  tiles=tiles)
+    assert one == pytest.approx(152 / 16)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n", [3, 5, 7])
+def test_schedule_replay_predicts_measured_batches(n):
+    """Prices measured on this GPU for the batch's own sequence lengths,
+    replayed through the launch's schedule, predict the measured fwd+bwd time
+    of the mixed Wan batch (3), the training-step batch with its 2 x 2 split
+    video (5) and the Fig. 2 batch of three split 720p videos and 228 images
+    (7) within 10% (the paper's profiler reports a makespan error of a few
+    percent, §V-B)."""
+    import synth
+    wl = synth.config(n)
+    r = profiler.validate_batch(wl.seqlens, wl.num_heads, wl.head_dim, tiles=wl.tiles() or None)
+    assert r["measured_ms"] > 0
+    assert abs(r["lpt_err"]) <= 0.10, r

@@ -252,6 +252,34 @@ def merge_bytes(wl, bf16_partials: bool = False) -> float:
     return total
 
 
+def e2e_timeline(steps):
+    """Where the end-to-end leg's time goes, from per-step event times (ms
+    from the start of the timed region): [h2d start, h2d end, compute start,
+    compute end, d2h start, d2h end] per step.  Reports the mean copy and
+    compute durations, the compute stream's idle time between steps (what the
+    copies failed to hide) and the share of copy time that ran while a
+    compute interval was open."""
+    if not steps:
+        return None
+    comp = [(s[2], s[3]) for s in steps]
+    copies = [(s[0], s[1]) for s in steps] + [(s[4], s[5]) for s in steps]
+
+    def overlap(a, b):
+        return max(0.0, min(a[1], b[1]) - max(a[0], b[0]))
+
+    copy_ms = sum(b - a for a, b in copies)
+    hidden = sum(overlap(c, k) for c in copies for k in comp)
+    idle = [comp[i + 1][0] - comp[i][1] for i in range(len(comp) - 1)]
+    n = len(steps)
+    return {"h2d_ms": round(sum(s[1] - s[0] for s in steps) / n, 2),
+            "d2h_ms": round(sum(s[5] - s[4] for s in steps) / n, 2),
+            "compute_ms": round(sum(b - a for a, b in comp) / n, 2),
+            "compute_idle_ms_between_steps": round(sum(idle) / max(1, len(idle)), 2),
+            "first_compute_start_ms": round(comp[0][0], 2),
+            "last_d2h_after_compute_ms": round(steps[-1][5] - steps[-1][3], 2),
+            "copy_time_overlapped": round(hidden / copy_ms, 4) if copy_ms > 0 else None}
+
+
 # ----------------------------------------------------------------- CPU oracle
 def oracle_sample(wl, inp, target_tokens: int, n_heads: int):
     """The first `n_heads` heads of the sequence of the workload nearest
@@ -500,27 +528,41 @@ def main():
             for e in ev[key]:
                 e.record(comp)
 
-        def e2e_step(i):
+        def timed_event(stream, marks):
+            if marks is not None:
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(stream)
+                marks.append(e)
+
+        def e2e_step(i, marks=None):
+            # marks (timed region only): h2d start/end, compute start/end,
+            # d2h start/end of this step, each recorded on its own stream
             sl = i % 2
             din, dout = dev_in[sl], dev_out[sl]
             with torch.cuda.stream(h2d):
                 h2d.wait_event(ev["comp"][sl])            # step i-2 no longer reads this slot
+                timed_event(h2d, marks)
                 for n in names_in:
                     din[n].copy_(host_in[n], non_blocking=True)
                 ev["h2d"][sl].record(h2d)
+                timed_event(h2d, marks)
             comp.wait_event(ev["h2d"][sl])
             comp.wait_event(ev["d2h"][sl])                # step i-2's results have left this slot
+            timed_event(comp, marks)
             zl.varlen_attn_fwd(din["q"], din["k"], din["v"], cu, cu, tiles=tiles, out=dout["o"],
                                lse=lse2[sl], workspace=fws, bf16_partials=args.bf16_partials)
             if step_bwd:
                 zl.varlen_attn_bwd(din["q"], din["k"], din["v"], dout["o"], lse2[sl], din["do"], cu, cu,
                                    tiles=tiles, dq=dout["dq"], dk=dout["dk"], dv=dout["dv"], workspace=bws)
             ev["comp"][sl].record(comp)
+            timed_event(comp, marks)
             with torch.cuda.stream(d2h):
                 d2h.wait_event(ev["comp"][sl])
+                timed_event(d2h, marks)
                 for n in names_out:
                     host_out[n].copy_(dout[n], non_blocking=True)
                 ev["d2h"][sl].record(d2h)
+                timed_event(d2h, marks)
 
         for i in range(2):
             e2e_step(i)
@@ -531,21 +573,23 @@ def main():
         e2e_sampler = ClockSampler(gpu_index_for_smi(local_rank))
         f0.record(comp)
         h2d.wait_event(f0)
+        marks = []
         for i in range(k_e2e):
-            e2e_step(i)
+            e2e_step(i, marks)
         comp.wait_stream(d2h)
         f1.record(comp)
         torch.cuda.synchronize()
         e2e_clocks = e2e_sampler.stop()
         barrier()
         ems = reduce_max_ms(f0.elapsed_time(f1), world, dev)
+        timeline = e2e_timeline([[f0.elapsed_time(e) for e in marks[6 * i:6 * i + 6]] for i in range(k_e2e)])
         bi = sum(t.numel() * t.element_size() for t in host_in.values())
         bo = sum(t.numel() * t.element_size() for t in host_out.values())
         e2e = {"value": round(job_tflops(world, k_e2e, flops_step, ems), 1),
                "unit": "TFLOP/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": k_e2e,
                "ms_per_step": round(ems / k_e2e, 3),
                "note": "copies of neighbouring steps overlap compute (2 copy streams, double-buffered device tensors)",
-               "clocks": e2e_clocks}
+               "timeline": timeline, "clocks": e2e_clocks}
         del dev_in, dev_out, host_in, host_out, lse2
 
     # ---------------- forward and fwd+bwd per configuration, each timed by itself

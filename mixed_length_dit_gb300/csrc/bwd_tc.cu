@@ -38,9 +38,12 @@
 // S^T / dP^T of the next block before the accumulation of the current one.
 //
 // Roles (512 threads, one CTA per SM): warps 0-7 softmax-grad (warp w reads
-// TMEM lanes 32*(w%4).. and query columns 32*(w/4)..) and the dV/dK epilogue,
-// warps 8-11 dQ drain, warp 12 TMA producer (4-stage Q/dO ring), warps 13-15
-// MMA issuers.  Every wait is bounded.
+// TMEM lanes 32*(w%4).. and query columns 32*(w/4)..), warps 8-11 dQ drain
+// and, after a key block's last query block, its dV/dK epilogue (so the
+// softmax-grad warps go straight on to the next item), warp 12 TMA producer
+// (4-stage Q/dO ring; once it knows the next item it prefetches that item's
+// K/V and first Q/dO tiles into L2), warps 13-15 MMA issuers.  Every wait is
+// bounded.
 // The grid holds one CTA per item, ordered longest-first by the host; the
 // resident CTA of an SM takes its own item, then the producer steals the next
 // unstarted one from the launch queue (cluster launch control) and hands its
@@ -155,7 +158,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(&sm->dq_drained, kDrainThreads);
     mbar_init(&sm->stage_full, kSgThreads);
     mbar_init(&sm->dkdv_full, 2);
-    mbar_init(&sm->dkdv_drained, kSgThreads);
+    mbar_init(&sm->dkdv_drained, kDrainThreads);
     ring_init(&sm->ring, kItemReaders);
     sm->abort_flag = 0;
     fence_mbar_init();
@@ -227,6 +230,23 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (!asked) ring_ask(&sm->ring);       // a key block without queries
         const int next = ring_answer(&sm->ring, steal_ph, args.n_items, abort_flag, &g_bwd_err,
                                      ERR_TIMEOUT_PRODUCER);
+        if (next >= 0) {
+          // The next item's K/V tiles (loaded once the current item's MMAs
+          // release K/V) and its first Q/dO block into L2 now, a few query
+          // blocks early, so that those loads hit L2.
+          const BwdWork nw = decode_bwd(args, next);
+          const BwdSeg& ns = args.segs[nw.seg];
+          const int nx0 = nw.h * HD;
+          const int nqb_next = (ns.q_len + kBQ - 1) / kBQ;
+          const int q_first = ns.q_row0 + (nw.kb % nqb_next) * kBQ;
+#pragma unroll
+          for (int c = 0; c < HD / 64; ++c) {
+            tma_prefetch_l2_2d(&tmK, nx0 + c * 64, ns.k_row0 + nw.kb * kBlockN);
+            tma_prefetch_l2_2d(&tmV, nx0 + c * 64, ns.k_row0 + nw.kb * kBlockN);
+            tma_prefetch_l2_2d(&tmQ, nx0 + c * 64, q_first);
+            tma_prefetch_l2_2d(&tmDO, nx0 + c * 64, q_first);
+          }
+        }
         if (next == -2 ||
             !ring_publish(&sm->ring, n, next, abort_flag, &g_bwd_err, ERR_TIMEOUT_PRODUCER) || next < 0)
           break;
@@ -367,9 +387,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int dw = warp - kDrainWarp0;                 // TMEM lane quadrant = d / 32
     const uint32_t lane_off = static_cast<uint32_t>(dw * 32) << 16;
     const bool active = dw * 32 < HD;
-    uint32_t g = 0;
+    const int nh = args.num_heads;
+    uint32_t g = 0, item_it = 0;
     bool ok = true;
-    for (uint32_t n = 0; ok; ++n) {
+    for (uint32_t n = 0; ok; ++n, ++item_it) {
       const int it = ring_take(&sm->ring, n, abort_flag, &g_bwd_err, ERR_TIMEOUT_OTHER, true);
       if (it < 0) break;
       const BwdWork w = decode_bwd(args, it);
@@ -422,6 +443,49 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           mbar_arrive(&sm->qd_empty[st]);
         }
       }
+      if (!ok) break;
+      // ------------------------------------------------ dV, dK of the key block
+      // Lane l of drain warp dw holds key row 32 dw + l of both accumulators;
+      // the next item's first dV / dK MMAs wait until all 128 rows are read.
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&sm->dkdv_full, item_it & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_OTHER))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int jrow = dw * 32 + lane;
+      const bool kv_ok = w.kb * kBlockN + jrow < sg.k_len;
+      const size_t krow = static_cast<size_t>(sg.k_row0) + static_cast<size_t>(w.kb * kBlockN + jrow);
+      __nv_bfloat16* dv_dst = reinterpret_cast<__nv_bfloat16*>(args.dv) + (krow * nh + w.h) * HD;
+      __nv_bfloat16* dk_dst = reinterpret_cast<__nv_bfloat16*>(args.dk) + (krow * nh + w.h) * HD;
+      const float sc = args.scale;
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t a[32], bb[32];
+        tmem_ld32(tDV + lane_off + 32 * c, a);
+        tmem_ld32(tDK + lane_off + 32 * c, bb);
+        tmem_wait_ld();
+        reg_fence(a);
+        reg_fence(bb);
+        if (kv_ok) {
+          uint4* dv4 = reinterpret_cast<uint4*>(dv_dst + 32 * c);
+          uint4* dk4 = reinterpret_cast<uint4*>(dk_dst + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            dv4[e] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * e + 0]), __uint_as_float(a[8 * e + 1])),
+                                pack_bf16x2(__uint_as_float(a[8 * e + 2]), __uint_as_float(a[8 * e + 3])),
+                                pack_bf16x2(__uint_as_float(a[8 * e + 4]), __uint_as_float(a[8 * e + 5])),
+                                pack_bf16x2(__uint_as_float(a[8 * e + 6]), __uint_as_float(a[8 * e + 7])));
+            dk4[e] = make_uint4(
+                pack_bf16x2(__uint_as_float(bb[8 * e + 0]) * sc, __uint_as_float(bb[8 * e + 1]) * sc),
+                pack_bf16x2(__uint_as_float(bb[8 * e + 2]) * sc, __uint_as_float(bb[8 * e + 3]) * sc),
+                pack_bf16x2(__uint_as_float(bb[8 * e + 4]) * sc, __uint_as_float(bb[8 * e + 5]) * sc),
+                pack_bf16x2(__uint_as_float(bb[8 * e + 6]) * sc, __uint_as_float(bb[8 * e + 7]) * sc));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sm->dkdv_drained);
     }
     if (lane == 0) bulk_wait_group0();        // the additions must land before exit
   } else {
@@ -430,11 +494,10 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int half = warp >> 2;
     const uint32_t lane_off = static_cast<uint32_t>(w4 * 32) << 16;
     const int jrow = w4 * 32 + lane;        // key row within the block
-    const int nh = args.num_heads;
     const float sl2 = args.scale_log2;
-    uint32_t item_it = 0, g = 0;
+    uint32_t g = 0;
     bool ok = true;
-    for (uint32_t n = 0; ok; ++n, ++item_it) {
+    for (uint32_t n = 0; ok; ++n) {
       const int it = ring_take(&sm->ring, n, abort_flag, &g_bwd_err, ERR_TIMEOUT_SOFTMAX, true);
       if (it < 0) break;
       const BwdWork w = decode_bwd(args, it);
@@ -505,42 +568,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_arrive(&sm->sg_done[b]);
       }
       if (!ok) break;
-      // ------------------------------------------------ dV, dK of the key block
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(&sm->dkdv_full, item_it & 1u, abort_flag, &g_bwd_err, ERR_TIMEOUT_SOFTMAX)))
-        break;
-      tc_fence_after();
-      const size_t krow = static_cast<size_t>(sg.k_row0 + w.kb * kBlockN + jrow);
-      __nv_bfloat16* dv_dst = reinterpret_cast<__nv_bfloat16*>(args.dv) + (krow * nh + w.h) * HD + half * (HD / 2);
-      __nv_bfloat16* dk_dst = reinterpret_cast<__nv_bfloat16*>(args.dk) + (krow * nh + w.h) * HD + half * (HD / 2);
-#pragma unroll
-      for (int c = 0; c < HD / 64; ++c) {
-        uint32_t a[32], bb[32];
-        tmem_ld32(tDV + lane_off + half * (HD / 2) + 32 * c, a);
-        tmem_ld32(tDK + lane_off + half * (HD / 2) + 32 * c, bb);
-        tmem_wait_ld();
-        reg_fence(a);
-        reg_fence(bb);
-        if (kv_ok) {
-          uint4* dv4 = reinterpret_cast<uint4*>(dv_dst + 32 * c);
-          uint4* dk4 = reinterpret_cast<uint4*>(dk_dst + 32 * c);
-          const float sc = args.scale;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            dv4[e] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * e + 0]), __uint_as_float(a[8 * e + 1])),
-                                pack_bf16x2(__uint_as_float(a[8 * e + 2]), __uint_as_float(a[8 * e + 3])),
-                                pack_bf16x2(__uint_as_float(a[8 * e + 4]), __uint_as_float(a[8 * e + 5])),
-                                pack_bf16x2(__uint_as_float(a[8 * e + 6]), __uint_as_float(a[8 * e + 7])));
-            dk4[e] = make_uint4(
-                pack_bf16x2(__uint_as_float(bb[8 * e + 0]) * sc, __uint_as_float(bb[8 * e + 1]) * sc),
-                pack_bf16x2(__uint_as_float(bb[8 * e + 2]) * sc, __uint_as_float(bb[8 * e + 3]) * sc),
-                pack_bf16x2(__uint_as_float(bb[8 * e + 4]) * sc, __uint_as_float(bb[8 * e + 5]) * sc),
-                pack_bf16x2(__uint_as_float(bb[8 * e + 6]) * sc, __uint_as_float(bb[8 * e + 7]) * sc));
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&sm->dkdv_drained);
     }
   }
 

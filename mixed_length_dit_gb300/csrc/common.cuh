@@ -113,6 +113,15 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// Brings one box of a tiled tensor into L2 (no shared memory, no completion
+// to wait for): a later tma_load_2d of the same box then hits L2.  Same
+// coordinate rules as tma_load_2d.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
+               : "memory");
+}
+
 // 2D tiled reduce-add of a shared-memory box into global memory (float32 add
 // for a float32 tensor map); tracked by the issuing thread's bulk async-group.
 // Coordinates must be non-negative; rows past the tensor's end are dropped.

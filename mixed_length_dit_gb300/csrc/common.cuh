@@ -122,6 +122,16 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32
                : "memory");
 }
 
+// 2D tiled store of a shared-memory box into global memory; tracked by the
+// issuing thread's bulk async-group.  Coordinates must be non-negative and x a
+// multiple of 16 bytes / element size; rows past the tensor's end are dropped.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
+      :: "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+      : "memory");
+}
+
 // 2D tiled reduce-add of a shared-memory box into global memory (float32 add
 // for a float32 tensor map); tracked by the issuing thread's bulk async-group.
 // Coordinates must be non-negative; rows past the tensor's end are dropped.

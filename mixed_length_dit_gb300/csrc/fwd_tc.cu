@@ -28,7 +28,12 @@
 //               P = 2^(S*scale*log2e - m) as bf16 over the S columns, and
 //               rescales the O row in TMEM when m grows by more than 2^8
 //               (lazy rescale; exactness holds for any m used consistently).
-//               After the last block it normalises O and writes O and LSE.
+//               After the last block it normalises O and writes O and LSE:
+//               a full 128-row tile of final rows is staged in the tile's
+//               own Q buffer (dead after the item's last S MMAs) and stored
+//               with TMA, and the producer loads the next item's Q there once
+//               the store has read it; partial tiles and shard partials are
+//               stored per thread.
 //   The two warpgroups take turns (an mbarrier per group, handed back and
 //   forth): the exponentials of one tile run while the tensor cores work on
 //   the other tile, instead of both groups competing for the SFU while the
@@ -150,7 +155,8 @@ __device__ __forceinline__ bool tile_present(const FwdSeg& sg, const FwdWork& w,
 template <int HD>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdArgs args) {
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+              const __grid_constant__ FwdArgs args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   auto* sm = reinterpret_cast<FwdSmem<HD>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -161,7 +167,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm->q_full[t], 1);
-      mbar_init(&sm->q_empty[t], 1);
+      mbar_init(&sm->q_empty[t], 2);           // the item's last S MMAs, and the epilogue done with q[t]
       mbar_init(&sm->s_full[t], 1);
       mbar_init(&sm->p_full[t], 128);
       mbar_init(&sm->o_full[t], 1);
@@ -242,6 +248,22 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (!asked) ring_ask(&sm->ring);       // an item without keys
         const int next = ring_answer(&sm->ring, steal_ph, args.n_items, abort_flag, &g_fwd_err,
                                      ERR_TIMEOUT_PRODUCER);
+        if (next >= 0) {
+          // The next item's Q tiles and first K/V tiles into L2 now, about two
+          // key blocks before they are loaded (Q once the current item's last
+          // S MMAs are done, K/V as ring stages free up), so those loads hit L2.
+          const FwdWork nw = decode_fwd(args, next);
+          const FwdSeg& ns = args.segs[nw.seg];
+          const int nx0 = nw.h * HD;
+#pragma unroll
+          for (int c = 0; c < HD / 64; ++c) {
+            for (int t = 0; t < 2; ++t)
+              if (tile_present(ns, nw, t))
+                tma_prefetch_l2_2d(&tmQ, nx0 + c * 64, ns.q_row0 + (2 * nw.qb + t) * kBlockM);
+            tma_prefetch_l2_2d(&tmK, nx0 + c * 64, ns.k_row0);
+            tma_prefetch_l2_2d(&tmV, nx0 + c * 64, ns.k_row0);
+          }
+        }
         if (next == -2 ||
             !ring_publish(&sm->ring, n, next, abort_flag, &g_fwd_err, ERR_TIMEOUT_PRODUCER) || next < 0)
           break;
@@ -471,7 +493,50 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const bool row_ok = q_local < sg.q_len;
       const float inv_l = 1.f / l_run;
       const float lse_val = (m_run + log2f(l_run)) * kLn2;
-      if (sg.slot < 0) {
+      const bool tma_tile = sg.slot < 0 && (qb + 1) * kBlockM <= sg.q_len;
+      // q[t] is free once the item's last S MMAs are done (o_full implies
+      // it); the epilogue of a full tile of final rows uses it as the staging
+      // area of its TMA store and releases it after the store has read it,
+      // any other epilogue releases it at once.
+      if (!tma_tile && row == 0) mbar_arrive(&sm->q_empty[t]);
+      if (tma_tile) {
+        // Each thread packs its row into q[t] in the Q tile's own layout
+        // (64-column boxes of [128 rows][128 B], 128-byte swizzle), and one
+        // thread stores the boxes with TMA: the rows of a tile are H*d
+        // elements apart, so per-thread stores would each touch their own
+        // lines.
+        const uint32_t r7 = static_cast<uint32_t>(row & 7);
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t oa[32];
+          tmem_ld32(tO + lane_off + c * 32, oa);
+          tmem_wait_ld();
+          reg_fence(oa);
+          uint8_t* box_row = sm->q[t] + (c >> 1) * (kBlockM * 128) + row * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t* src = oa + 8 * k;
+            uint4 pk;
+            pk.x = pack_bf16x2(__uint_as_float(src[0]) * inv_l, __uint_as_float(src[1]) * inv_l);
+            pk.y = pack_bf16x2(__uint_as_float(src[2]) * inv_l, __uint_as_float(src[3]) * inv_l);
+            pk.z = pack_bf16x2(__uint_as_float(src[4]) * inv_l, __uint_as_float(src[5]) * inv_l);
+            pk.w = pack_bf16x2(__uint_as_float(src[6]) * inv_l, __uint_as_float(src[7]) * inv_l);
+            const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + k);
+            *reinterpret_cast<uint4*>(box_row + ((chunk ^ r7) << 4)) = pk;
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1 + t, 128);
+        if (row == 0) {
+#pragma unroll
+          for (int c2 = 0; c2 < HD / 64; ++c2)
+            tma_store_2d(&tmO, sm->q[t] + c2 * (kBlockM * 128), w.h * HD + c2 * 64, sg.q_row0 + qb * kBlockM);
+          bulk_commit_group();
+          bulk_wait_group_read0();             // q[t] read: the next item's Q may land there
+          mbar_arrive(&sm->q_empty[t]);
+        }
+        args.lse[static_cast<size_t>(w.h) * args.lse_stride + sg.q_row0 + q_local] = lse_val;
+      } else if (sg.slot < 0) {
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.o) +
                              (static_cast<size_t>(sg.q_row0 + q_local) * nh + w.h) * HD;
 #pragma unroll 1
@@ -539,6 +604,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
       }
     }
+    // this group's output stores must have completed before the CTA exits
+    if (row == 0) bulk_wait_group0();
   }
 
   // ---------------------------------------------------------------- teardown
@@ -552,12 +619,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
 template <int HD>
 cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                      const FwdArgs& args, cudaStream_t stream) {
+                      const CUtensorMap& to, const FwdArgs& args, cudaStream_t stream) {
   const size_t smem = sizeof(FwdSmem<HD>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  fwd_tc_kernel<HD><<<args.n_items, kFwdThreads, smem, stream>>>(tq, tk, tv, args);
+  fwd_tc_kernel<HD><<<args.n_items, kFwdThreads, smem, stream>>>(tq, tk, tv, to, args);
   return cudaGetLastError();
 }
 
@@ -568,9 +635,10 @@ size_t fwd_tc_smem_bytes(int head_dim) {
 }
 
 cudaError_t launch_fwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const FwdArgs& args, cudaStream_t stream) {
-  if (head_dim == 64) return launch_tc<64>(tq, tk, tv, args, stream);
-  if (head_dim == 128) return launch_tc<128>(tq, tk, tv, args, stream);
+                          const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& args,
+                          cudaStream_t stream) {
+  if (head_dim == 64) return launch_tc<64>(tq, tk, tv, to, args, stream);
+  if (head_dim == 128) return launch_tc<128>(tq, tk, tv, to, args, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -99,8 +99,11 @@ struct BwdArgs {
 // Each returns the CUDA error of the launch (cudaSuccess when enqueued).
 // The tensor-core kernels are launched with one CTA per work item
 // (args.n_items): the CTAs resident at a time steal the unstarted ones.
+// to: bf16 map of the output o with the same box shape as tq (the kernel
+// stores full 128-row tiles of final rows through it).
 cudaError_t launch_fwd_tc(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const FwdArgs& args, cudaStream_t stream);
+                          const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& args,
+                          cudaStream_t stream);
 cudaError_t launch_fwd_f32(int head_dim, const float* q, const float* k, const float* v,
                            const FwdArgs& args, cudaStream_t stream);
 cudaError_t launch_merge(int head_dim, const MergeArgs& args, int num_sms, cudaStream_t stream);

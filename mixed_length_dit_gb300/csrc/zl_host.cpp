@@ -625,10 +625,10 @@ zl_status zl_varlen_attn_fwd_ex(const void* q, const void* k, const void* v, con
       if (st != ZL_OK) return st;
     }
   }
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (dtype == ZL_BF16) {
     if (!make_map(&mq, q, plan.tq, num_heads, head_dim) || !make_map(&mk, k, plan.tk, num_heads, head_dim) ||
-        !make_map(&mv, v, plan.tk, num_heads, head_dim))
+        !make_map(&mv, v, plan.tk, num_heads, head_dim) || !make_map(&mo, o, plan.tq, num_heads, head_dim))
       return ZL_ECUDA;
   }
   for (size_t first = 0; first < segs.size(); first += kMaxSegs) {
@@ -636,7 +636,7 @@ zl_status zl_varlen_attn_fwd_ex(const void* q, const void* k, const void* v, con
     if (!fill_args(&args, segs, first, last, dtype == ZL_BF16 ? zl::kFwdRowsPerItem : kBlockM)) return ZL_EINVAL;
     if (args.n_items == 0) continue;
     if (dtype == ZL_BF16) {
-      st = launch_counted("fwd_tc", s, [&] { return zl::launch_fwd_tc(head_dim, mq, mk, mv, args, s); });
+      st = launch_counted("fwd_tc", s, [&] { return zl::launch_fwd_tc(head_dim, mq, mk, mv, mo, args, s); });
     } else {
       st = launch_counted("fwd_f32", s, [&] {
         return zl::launch_fwd_f32(head_dim, static_cast<const float*>(q), static_cast<const float*>(k),

@@ -95,6 +95,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return mbar_wait_limit(bar, parity, abort_flag, err, code, ZL_WAIT_LIMIT_NS);
 }
 
+// A barrier among the threads of one role, built on an mbarrier initialised
+// with their count, so that its wait is bounded like every other wait: a
+// thread whose role gave up (abort flag) never blocks the others for good.
+// Every participant calls it the same number of times; `uses` is the
+// caller's count of its earlier calls on this barrier.
+__device__ __forceinline__ bool mbar_sync(uint64_t* bar, uint32_t& uses, volatile int* abort_flag,
+                                          uint32_t* err, uint32_t code) {
+  mbar_arrive(bar);
+  const bool ok = mbar_wait(bar, uses & 1u, abort_flag, err, code);
+  ++uses;
+  return ok;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");

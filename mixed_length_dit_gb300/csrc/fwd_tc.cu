@@ -74,6 +74,8 @@ struct FwdSmem {
   uint64_t kv_full[kFwdStages], kv_empty[kFwdStages];
   uint64_t s_full[2], p_full[2], o_full[2];
   uint64_t turn[2];                            // softmax group t may run its next block
+  uint64_t grp_sync[2];                        // barrier of softmax group t's 128 threads
+  uint32_t grp_uses[2][128];                   // per thread: its earlier arrivals on grp_sync[t]
   ItemRing ring;                               // work items, producer -> the other roles
   uint32_t tmem_base;
   int abort_flag;
@@ -172,6 +174,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_init(&sm->p_full[t], 128);
       mbar_init(&sm->o_full[t], 1);
       mbar_init(&sm->turn[t], 128);
+      mbar_init(&sm->grp_sync[t], 128);
     }
     for (int s = 0; s < kFwdStages; ++s) {
       mbar_init(&sm->kv_full[s], 1);
@@ -360,6 +363,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const float sl2 = args.scale_log2;
     const int nh = args.num_heads;
     uint32_t blk_it = 0, q_it = 0, turn_it = 0;
+    // this thread's count of grp_sync[t] phases, kept in shared memory so it
+    // takes no register across the block loop
+    sm->grp_uses[t][row] = 0;
     // group 1 hands the first turn to group 0
     if (t == 1) mbar_arrive(&sm->turn[0]);
     for (uint32_t n = 0;; ++n) {
@@ -526,8 +532,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           }
         }
         fence_proxy_async_smem();
-        named_bar_sync(1 + t, 128);
+        // only the storing thread waits for the group's rows; the others
+        // just arrive (and count the phase)
+        mbar_arrive(&sm->grp_sync[t]);
+        const uint32_t phase = sm->grp_uses[t][row]++;
         if (row == 0) {
+          if (!mbar_wait(&sm->grp_sync[t], phase & 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_SOFTMAX)) break;
 #pragma unroll
           for (int c2 = 0; c2 < HD / 64; ++c2)
             tma_store_2d(&tmO, sm->q[t] + c2 * (kBlockM * 128), w.h * HD + c2 * 64, sg.q_row0 + qb * kBlockM);
@@ -594,10 +604,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // of kv chunks of this (query block, head) merges them into o / lse.
         if (!args.fused_merge) continue;
         __threadfence();
-        named_bar_sync(1 + t, 128);
+        uint32_t u = sm->grp_uses[t][row];
+        if (!__all_sync(0xffffffffu, mbar_sync(&sm->grp_sync[t], u, abort_flag, &g_fwd_err, ERR_TIMEOUT_SOFTMAX)))
+          break;
         if (row == 0)
           sm->is_last[t] = atomicAdd(args.counters + sg.counter0 + qb * nh + w.h, 1) == sg.n_kv - 1;
-        named_bar_sync(1 + t, 128);
+        const bool synced =
+            __all_sync(0xffffffffu, mbar_sync(&sm->grp_sync[t], u, abort_flag, &g_fwd_err, ERR_TIMEOUT_SOFTMAX));
+        sm->grp_uses[t][row] = u;
+        if (!synced) break;
         if (sm->is_last[t]) {
           __threadfence();
           if (row_ok) merge_tile_row<HD>(args, sg, w.h, q_local);

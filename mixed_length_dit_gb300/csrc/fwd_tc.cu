@@ -439,30 +439,26 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         l_run *= alpha;
         const float neg_m = -m_run;
-        // exponent arguments and row sums on float32 pairs; each half of P
+        // exponent arguments and row sums on float32 pairs; each quarter of P
         // goes to TMEM as soon as it is packed, freeing its S registers
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         const uint64_t negm2 = f2_pack(neg_m, neg_m);
         uint64_t acc[2] = {0ull, 0ull};
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t p[32];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t p[16];
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int c = 2 * hf + cc;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1])),
-                                        sl2x2, negm2);
-              float x0, x1;
-              f2_unpack(x, x0, x1);
-              const float a = fast_exp2(x0);
-              const float b = fast_exp2(x1);
-              acc[i & 1] = f2_add(acc[i & 1], f2_pack(a, b));
-              p[cc * 16 + i] = pack_bf16x2(a, b);
-            }
+          for (int i = 0; i < 16; ++i) {
+            const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1])),
+                                      sl2x2, negm2);
+            float x0, x1;
+            f2_unpack(x, x0, x1);
+            const float a = fast_exp2(x0);
+            const float b = fast_exp2(x1);
+            acc[i & 1] = f2_add(acc[i & 1], f2_pack(a, b));
+            p[i] = pack_bf16x2(a, b);
           }
-          tmem_st32(tS + lane_off + 32 * hf, p);
+          tmem_st16(tS + lane_off + 16 * c, p);
         }
         float ls0, ls1;
         f2_unpack(f2_add(acc[0], acc[1]), ls0, ls1);

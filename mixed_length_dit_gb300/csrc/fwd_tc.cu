@@ -12,8 +12,9 @@
 //
 // The two query tiles of an item share every K_j / V_j tile that the producer
 // brings into shared memory.  Per CTA (352 threads):
-//   warp 8      TMA producer: the two Q tiles once per item, then K_j / V_j
-//               through a four-stage ring (128-byte swizzle, 64-column boxes).
+//   warp 8      TMA producer: K_0, the two Q tiles once per item, then V_0
+//               and the further K_j / V_j through a four-stage ring (128-byte
+//               swizzle, 64-column boxes).
 //               It also steals the next item and hands it to the other roles
 //               through a two-slot ring in shared memory.
 //   warps 9,10  MMA issuers, one thread each, one per query tile t:
@@ -210,19 +211,26 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const int nkb = (sg.k_len + kBlockN - 1) / kBlockN;
         const int x0 = w.h * HD;
         bool asked = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (!tile_present(sg, w, t)) continue;
-          if (!mbar_wait(&sm->q_empty[t], (q_it[t] & 1u) ^ 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_PRODUCER)) {
-            ok = false;
-            break;
-          }
-          ++q_it[t];
-          mbar_arrive_expect_tx(&sm->q_full[t], kBlockM * HD * 2);
-          const int q_row = sg.q_row0 + (2 * w.qb + t) * kBlockM;
+        // The item's Q tiles, each once the previous item's tile has released
+        // its buffer (its last S MMAs and its output store).  Issued after
+        // K_0, whose ring stage frees earlier: tile 0's first S then does not
+        // wait for tile 1's epilogue of the previous item.
+        auto load_q = [&]() {
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (!tile_present(sg, w, t)) continue;
+            if (!mbar_wait(&sm->q_empty[t], (q_it[t] & 1u) ^ 1u, abort_flag, &g_fwd_err, ERR_TIMEOUT_PRODUCER)) {
+              ok = false;
+              break;
+            }
+            ++q_it[t];
+            mbar_arrive_expect_tx(&sm->q_full[t], kBlockM * HD * 2);
+            const int q_row = sg.q_row0 + (2 * w.qb + t) * kBlockM;
 #pragma unroll
-          for (int c = 0; c < HD / 64; ++c)
-            tma_load_2d(sm->q[t] + c * kBlockM * 128, &tmQ, &sm->q_full[t], x0 + c * 64, q_row);
-        }
+            for (int c = 0; c < HD / 64; ++c)
+              tma_load_2d(sm->q[t] + c * kBlockM * 128, &tmQ, &sm->q_full[t], x0 + c * 64, q_row);
+          }
+        };
+        if (nkb == 0) load_q();
         for (int j = 0; j < nkb && ok; ++j) {
           if (j == nkb - 1) {
             // the item's last K/V tiles are next: ask for the following item
@@ -245,6 +253,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               tma_load_2d(sm->kv[st] + c * kBlockN * 128, map, &sm->kv_full[st], x0 + c * 64,
                           sg.k_row0 + j * kBlockN);
             ++kv_it;
+            if (j == 0 && kv == 0) {
+              load_q();
+              if (!ok) break;
+            }
           }
         }
         if (!ok) break;

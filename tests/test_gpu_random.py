@@ -22,7 +22,7 @@ from _helpers import TOL_GRAD_REL_L2, TOL_LSE, TOL_O_BF16, f64, rel_l2
 
 pytestmark = pytest.mark.gpu
 
-N_DRAWS = 24
+N_DRAWS = 64
 
 
 def _draw(rng):

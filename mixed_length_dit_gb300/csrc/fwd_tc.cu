@@ -407,18 +407,56 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         uint32_t s[4][32];
         const int valid = sg.k_len - j * kBlockN;
         float m_raw;
+        // Speculation on a full block after the first: the exponentials of
+        // the first 32 columns are computed with the running max while the
+        // other 96 columns load.  They stand if the block does not raise the
+        // max past the lazy-rescale threshold (the running max is then kept,
+        // exactly as without speculation); otherwise the block is redone from
+        // TMEM, where S is still intact.
+        bool spec_done = false;
+        uint32_t p0[16];
+        uint64_t acc[2] = {0ull, 0ull};
         if (valid >= kBlockN) {
           // full block: the reducing TMEM load returns each 32-column max
           float r[4];
+          r[0] = tmem_ld32_max(tS + lane_off, s[0]);
+          tmem_wait_ld();
+          reg_fence(s[0]);
+          reg_fence_f(r[0]);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) r[c] = tmem_ld32_max(tS + lane_off + c * 32, s[c]);
+          for (int c = 1; c < 4; ++c) r[c] = tmem_ld32_max(tS + lane_off + c * 32, s[c]);
+          const bool spec = j > 0 && __all_sync(0xffffffffu, r[0] * sl2 <= m_run + kRescaleThreshold);
+          if (spec) {
+            const uint64_t sl2x2 = f2_pack(sl2, sl2);
+            const uint64_t negm2 = f2_pack(-m_run, -m_run);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[0][2 * i]), __uint_as_float(s[0][2 * i + 1])),
+                                        sl2x2, negm2);
+              float x0, x1;
+              f2_unpack(x, x0, x1);
+              const float a = fast_exp2(x0);
+              const float b = fast_exp2(x1);
+              acc[i & 1] = f2_add(acc[i & 1], f2_pack(a, b));
+              p0[i] = pack_bf16x2(a, b);
+            }
+          }
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 1; c < 4; ++c) {
             reg_fence(s[c]);
             reg_fence_f(r[c]);
           }
           m_raw = fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3]));
+          spec_done = spec && __all_sync(0xffffffffu, m_raw * sl2 <= m_run + kRescaleThreshold);
+          if (!spec_done) {
+            // (rare) the first 32 columns again, for the exact path below
+            acc[0] = 0ull;
+            acc[1] = 0ull;
+            tmem_ld32(tS + lane_off, s[0]);
+            tmem_wait_ld();
+            reg_fence(s[0]);
+          }
         } else {
           // last block of the segment: columns past its keys do not count
 #pragma unroll
@@ -455,9 +493,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // goes to TMEM as soon as it is packed, freeing its S registers
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         const uint64_t negm2 = f2_pack(neg_m, neg_m);
-        uint64_t acc[2] = {0ull, 0ull};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          if (c == 0 && spec_done) {
+            tmem_st16(tS + lane_off, p0);
+            continue;
+          }
           uint32_t p[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {

@@ -14,7 +14,7 @@ import torch
 import oracle
 import synth
 import mixed_length_dit_gb300 as zl
-from _helpers import TOL_FP32, TOL_LSE, TOL_O_BF16, f64, sample_rows
+from _helpers import TOL_FP32, TOL_GRAD_REL_L2, TOL_LSE, TOL_O_BF16, f64, rel_l2, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -84,6 +84,42 @@ def test_ragged_edges(hd):
     cu = wl.cu_seqlens()
     _full_check(inp["q"], inp["k"], inp["v"], cu, cu, o, lse, TOL_O_BF16, TOL_LSE)
 
+
+
+@pytest.mark.parametrize("case", ["block", "inner", "growing"])
+@pytest.mark.parametrize("split", [False, True])
+def test_running_max_jumps(case, split):
+    """Keys whose scores jump after the first key block, so that the running
+    maximum of nearly every query row grows by more than the lazy-rescale
+    threshold (2^8) in the middle of the sequence, which N(0, 1) inputs never
+    do: a whole 128-key block scaled by 6 (its first 32 columns already
+    exceed the threshold), only keys 40-99 of a block scaled by 6 (the
+    exponentials of the block's first 32 columns start on the old maximum
+    and must be redone), and every block scaled by 1.5^j (repeated
+    rescales, the last one in the partial block).  Forward O and LSE against
+    the oracle, whole and as a 2 x 2 tile grid, then the backward's
+    gradients from that O and LSE."""
+    L = 1000
+    wl = synth.Workload("jumps", [L, 300], 2, 128)
+    inp = synth.make_inputs(wl, seed=11, device="cuda")
+    k = inp["k"].float()
+    if case == "block":
+        k[384:512] *= 6
+    elif case == "inner":
+        k[384 + 40:384 + 100] *= 6
+    else:
+        for j in range(8):
+            k[128 * j:128 * (j + 1)] *= 1.5 ** j
+    inp["k"] = k.to(torch.bfloat16)
+    tiles = synth.grid_tiles(0, L, L, 2, 2) if split else None
+    cu = wl.cu_seqlens()
+    o, lse = _run(inp, wl, tiles)
+    _full_check(inp["q"], inp["k"], inp["v"], cu, cu, o, lse, TOL_O_BF16, TOL_LSE)
+    dq, dk, dv = zl.varlen_attn_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], cu, cu, tiles=tiles)
+    zl.sync_check()
+    refs = oracle.varlen_attn_bwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["do"]), cu, cu)
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        assert rel_l2(f64(got), ref) <= TOL_GRAD_REL_L2, (name, rel_l2(f64(got), ref))
 
 def test_different_query_and_key_lengths():
     cu_q = [0, 5, 200, 330]

@@ -255,14 +255,16 @@ def merge_bytes(wl, bf16_partials: bool = False) -> float:
 def e2e_timeline(steps):
     """Where the end-to-end leg's time goes, from per-step event times (ms
     from the start of the timed region): [h2d start, h2d end, compute start,
-    compute end, d2h start, d2h end] per step.  Reports the mean copy and
-    compute durations, the compute stream's idle time between steps (what the
-    copies failed to hide) and the share of copy time that ran while a
-    compute interval was open."""
+    compute end, then the start and end of each device-to-host copy group]
+    per step (the output O leaves after the forward, the gradients after the
+    backward).  Reports the mean copy and compute durations, the compute
+    stream's idle time between steps (what the copies failed to hide) and the
+    share of copy time that ran while a compute interval was open."""
     if not steps:
         return None
     comp = [(s[2], s[3]) for s in steps]
-    copies = [(s[0], s[1]) for s in steps] + [(s[4], s[5]) for s in steps]
+    outs = [[(s[i], s[i + 1]) for i in range(4, len(s) - 1, 2)] for s in steps]
+    copies = [(s[0], s[1]) for s in steps] + [c for o in outs for c in o]
 
     def overlap(a, b):
         return max(0.0, min(a[1], b[1]) - max(a[0], b[0]))
@@ -272,11 +274,11 @@ def e2e_timeline(steps):
     idle = [comp[i + 1][0] - comp[i][1] for i in range(len(comp) - 1)]
     n = len(steps)
     return {"h2d_ms": round(sum(s[1] - s[0] for s in steps) / n, 2),
-            "d2h_ms": round(sum(s[5] - s[4] for s in steps) / n, 2),
+            "d2h_ms": round(sum(b - a for o in outs for a, b in o) / n, 2),
             "compute_ms": round(sum(b - a for a, b in comp) / n, 2),
             "compute_idle_ms_between_steps": round(sum(idle) / max(1, len(idle)), 2),
             "first_compute_start_ms": round(comp[0][0], 2),
-            "last_d2h_after_compute_ms": round(steps[-1][5] - steps[-1][3], 2),
+            "last_d2h_after_compute_ms": round(steps[-1][-1] - steps[-1][3], 2),
             "copy_time_overlapped": round(hidden / copy_ms, 4) if copy_ms > 0 else None}
 
 
@@ -510,7 +512,9 @@ def main():
     # four results (O, dQ, dK, dV) back out, all inside the timed region.  The
     # copies of neighbouring steps overlap the compute of the current one
     # (inputs and outputs double-buffered on the device, one stream each for
-    # host-to-device and device-to-host copies).
+    # host-to-device and device-to-host copies); within a step the forward
+    # starts once q, k and v are in (dO follows) and O leaves while the
+    # backward runs.
     e2e = None
     if not args.no_e2e:
         k_e2e = max(2, args.steps)
@@ -523,7 +527,7 @@ def main():
         lse2 = [torch.empty_like(lse) for _ in range(2)]
         comp = torch.cuda.current_stream()
         h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
-        ev = {key: [torch.cuda.Event() for _ in range(2)] for key in ("h2d", "comp", "d2h")}
+        ev = {key: [torch.cuda.Event() for _ in range(2)] for key in ("qkv", "h2d", "fwd", "comp", "d2h")}
         for key in ev:
             for e in ev[key]:
                 e.record(comp)
@@ -535,31 +539,40 @@ def main():
                 marks.append(e)
 
         def e2e_step(i, marks=None):
-            # marks (timed region only): h2d start/end, compute start/end,
-            # d2h start/end of this step, each recorded on its own stream
+            # marks (timed region only): h2d start/end, compute start/end, the
+            # O copy's start/end and the gradients' copy start/end of this
+            # step, each recorded on its own stream
             sl = i % 2
             din, dout = dev_in[sl], dev_out[sl]
             with torch.cuda.stream(h2d):
                 h2d.wait_event(ev["comp"][sl])            # step i-2 no longer reads this slot
                 timed_event(h2d, marks)
-                for n in names_in:
+                for n in ("q", "k", "v"):
                     din[n].copy_(host_in[n], non_blocking=True)
+                ev["qkv"][sl].record(h2d)                 # the forward's inputs are in
+                din["do"].copy_(host_in["do"], non_blocking=True)
                 ev["h2d"][sl].record(h2d)
                 timed_event(h2d, marks)
-            comp.wait_event(ev["h2d"][sl])
+            comp.wait_event(ev["qkv"][sl])
             comp.wait_event(ev["d2h"][sl])                # step i-2's results have left this slot
             timed_event(comp, marks)
             zl.varlen_attn_fwd(din["q"], din["k"], din["v"], cu, cu, tiles=tiles, out=dout["o"],
                                lse=lse2[sl], workspace=fws, bf16_partials=args.bf16_partials)
+            ev["fwd"][sl].record(comp)
             if step_bwd:
+                comp.wait_event(ev["h2d"][sl])            # dO is in
                 zl.varlen_attn_bwd(din["q"], din["k"], din["v"], dout["o"], lse2[sl], din["do"], cu, cu,
                                    tiles=tiles, dq=dout["dq"], dk=dout["dk"], dv=dout["dv"], workspace=bws)
             ev["comp"][sl].record(comp)
             timed_event(comp, marks)
             with torch.cuda.stream(d2h):
+                d2h.wait_event(ev["fwd"][sl])             # O leaves while the backward runs
+                timed_event(d2h, marks)
+                host_out["o"].copy_(dout["o"], non_blocking=True)
+                timed_event(d2h, marks)
                 d2h.wait_event(ev["comp"][sl])
                 timed_event(d2h, marks)
-                for n in names_out:
+                for n in names_out[1:]:
                     host_out[n].copy_(dout[n], non_blocking=True)
                 ev["d2h"][sl].record(d2h)
                 timed_event(d2h, marks)
@@ -582,13 +595,14 @@ def main():
         e2e_clocks = e2e_sampler.stop()
         barrier()
         ems = reduce_max_ms(f0.elapsed_time(f1), world, dev)
-        timeline = e2e_timeline([[f0.elapsed_time(e) for e in marks[6 * i:6 * i + 6]] for i in range(k_e2e)])
+        timeline = e2e_timeline([[f0.elapsed_time(e) for e in marks[8 * i:8 * i + 8]] for i in range(k_e2e)])
         bi = sum(t.numel() * t.element_size() for t in host_in.values())
         bo = sum(t.numel() * t.element_size() for t in host_out.values())
         e2e = {"value": round(job_tflops(world, k_e2e, flops_step, ems), 1),
                "unit": "TFLOP/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": k_e2e,
                "ms_per_step": round(ems / k_e2e, 3),
-               "note": "copies of neighbouring steps overlap compute (2 copy streams, double-buffered device tensors)",
+               "note": ("copies of neighbouring steps overlap compute (2 copy streams, double-buffered device "
+                        "tensors); the forward starts once q, k, v are in, O leaves during the backward"),
                "timeline": timeline, "clocks": e2e_clocks}
         del dev_in, dev_out, host_in, host_out, lse2
 

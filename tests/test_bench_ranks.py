@@ -166,15 +166,19 @@ def test_clock_sampler_cleans_up_without_nvidia_smi(monkeypatch):
 
 
 def test_e2e_timeline_summary():
-    """Two steps: copies of 10 ms each, compute of 100 ms; the second
+    """Two steps: input copies of 10 ms, compute of 100 ms; the second
     step's input copy runs during the first compute, its compute starts 5 ms
-    after the first one ends; the last output copy runs after all compute."""
-    steps = [[0, 10, 10, 110, 110, 120],
-             [20, 30, 115, 215, 215, 225]]
+    after the first one ends.  Each step's output leaves in two groups: O
+    (4 ms, during the compute) and the gradients (6 ms, after it); the last
+    step's gradients leave after all compute."""
+    steps = [[0, 10, 10, 110, 50, 54, 110, 116],
+             [20, 30, 115, 215, 155, 159, 215, 221]]
     t = bench.e2e_timeline(steps)
     assert t["h2d_ms"] == 10 and t["d2h_ms"] == 10 and t["compute_ms"] == 100
     assert t["compute_idle_ms_between_steps"] == 5
-    assert t["first_compute_start_ms"] == 10 and t["last_d2h_after_compute_ms"] == 10
-    # hidden: step 2's h2d (20..30) overlaps compute 1; step 1's d2h (110..120) overlaps compute 2 for 5 ms
-    assert t["copy_time_overlapped"] == round((10 + 5) / 40, 4)
+    assert t["first_compute_start_ms"] == 10 and t["last_d2h_after_compute_ms"] == 6
+    # hidden: step 2's h2d (20..30) overlaps compute 1 (10 ms); both O copies
+    # overlap their compute (8 ms); step 1's gradients (110..116) overlap
+    # compute 2 for 1 ms
+    assert t["copy_time_overlapped"] == round((10 + 8 + 1) / 40, 4)
     assert bench.e2e_timeline([]) is None

@@ -40,6 +40,45 @@ def _check_tensor(t, name):
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
 
 
+def _last(cu) -> int:
+    vals = cu.tolist() if hasattr(cu, "tolist") else list(cu)
+    if not vals:
+        raise ValueError("cu_seqlens must have at least one entry")
+    return int(vals[-1])
+
+
+def _check_like(t, name, shape, dtype, device):
+    """t must be a contiguous CUDA tensor of exactly this shape, dtype and
+    device: the library receives only its pointer and writes or reads the
+    sizes that the batch implies."""
+    _check_tensor(t, name)
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != device:
+        raise ValueError(f"{name} must be {tuple(shape)} {dtype} on {device}, "
+                         f"got {tuple(t.shape)} {t.dtype} on {t.device}")
+
+
+def _check_qkv(q, k, v, cu_seqlens_q, cu_seqlens_k):
+    """q [Tq, H, d], k and v [Tk, H, d] of one dtype on one device, with Tq
+    and Tk the last entries of the cu_seqlens (the packed layout of the C
+    ABI), so that no tensor map or row index reaches past an allocation."""
+    _check_tensor(q, "q")
+    if q.dim() != 3:
+        raise ValueError("q must be [Tq, H, d]")
+    tq, nh, hd = q.shape
+    if tq != _last(cu_seqlens_q):
+        raise ValueError(f"q has {tq} rows, cu_seqlens_q ends at {_last(cu_seqlens_q)}")
+    _check_like(k, "k", (_last(cu_seqlens_k), nh, hd), q.dtype, q.device)
+    _check_like(v, "v", k.shape, q.dtype, q.device)
+    return tq, nh, hd
+
+
+def _workspace_bytes(workspace) -> int:
+    if workspace is None:
+        return 0
+    _check_tensor(workspace, "workspace")
+    return workspace.numel() * workspace.element_size()
+
+
 def fwd_workspace_bytes(cu_seqlens_q, cu_seqlens_k, num_heads, head_dim, tiles=None) -> int:
     lib = _lib.load()
     cq, nq = _lib.int32_array(cu_seqlens_q)
@@ -112,14 +151,14 @@ def varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k=None, tiles=None, softma
     lib = _lib.load()
     if cu_seqlens_k is None:
         cu_seqlens_k = cu_seqlens_q
-    for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check_tensor(t, n)
-    tq, nh, hd = q.shape
+    tq, nh, hd = _check_qkv(q, k, v, cu_seqlens_q, cu_seqlens_k)
     scale = 1.0 / math.sqrt(hd) if softmax_scale is None else float(softmax_scale)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((nh, tq), dtype=torch.float32, device=q.device)
+    _check_like(out, "out", q.shape, q.dtype, q.device)
+    _check_like(lse, "lse", (nh, tq), torch.float32, q.device)
     if workspace is None:
         workspace = alloc_workspace(fwd_workspace_bytes(cu_seqlens_q, cu_seqlens_k, nh, hd, tiles), q.device)
     cq, nq = _lib.int32_array(cu_seqlens_q)
@@ -127,7 +166,7 @@ def varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k=None, tiles=None, softma
     if nq != nk:
         raise ValueError("cu_seqlens_q and cu_seqlens_k differ in length")
     ta, nt = _lib.tile_array(tiles)
-    ws_bytes = workspace.numel() if workspace is not None else 0
+    ws_bytes = _workspace_bytes(workspace)
     flags = (_lib.ZL_FWD_FUSED_MERGE if fused_merge else 0) | (_lib.ZL_FWD_BF16_PARTIALS if bf16_partials else 0)
     st = lib.zl_varlen_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), cq, ck, nq - 1, nh, hd, _dtype_code(q),
                                    scale, ta, nt, _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
@@ -142,19 +181,23 @@ def varlen_attn_bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k=None, tile
     lib = _lib.load()
     if cu_seqlens_k is None:
         cu_seqlens_k = cu_seqlens_q
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (lse, "lse"), (dout, "dout")):
-        _check_tensor(t, n)
-    tq, nh, hd = q.shape
+    tq, nh, hd = _check_qkv(q, k, v, cu_seqlens_q, cu_seqlens_k)
+    _check_like(o, "o", q.shape, q.dtype, q.device)
+    _check_like(dout, "dout", q.shape, q.dtype, q.device)
+    _check_like(lse, "lse", (nh, tq), torch.float32, q.device)
     scale = 1.0 / math.sqrt(hd) if softmax_scale is None else float(softmax_scale)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _check_like(dq, "dq", q.shape, q.dtype, q.device)
+    _check_like(dk, "dk", k.shape, q.dtype, q.device)
+    _check_like(dv, "dv", k.shape, q.dtype, q.device)
     if workspace is None:
         workspace = alloc_workspace(bwd_workspace_bytes(cu_seqlens_q, cu_seqlens_k, nh, hd), q.device)
     cq, nq = _lib.int32_array(cu_seqlens_q)
     ck, _ = _lib.int32_array(cu_seqlens_k)
     ta, nt = _lib.tile_array(tiles)
-    ws_bytes = workspace.numel() if workspace is not None else 0
+    ws_bytes = _workspace_bytes(workspace)
     st = lib.zl_varlen_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), cq, ck,
                                 nq - 1, nh, hd, _dtype_code(q), scale, ta, nt, _ptr(dq), _ptr(dk),
                                 _ptr(dv), _ptr(workspace), ws_bytes, _stream_handle(stream))
@@ -168,20 +211,31 @@ def lse_merge(o_partial, lse_partial, rows=None, out_dtype=torch.bfloat16, out=N
     lse_partial [P, H, R] (float32) into (o [rows, H, d], lse [H, rows])."""
     lib = _lib.load()
     _check_tensor(o_partial, "o_partial")
-    _check_tensor(lse_partial, "lse_partial")
+    if o_partial.dim() != 4 or o_partial.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("o_partial must be [P, R, H, d] float32 or bf16")
     n_parts, part_rows, nh, hd = o_partial.shape
+    dev = o_partial.device
+    _check_like(lse_partial, "lse_partial", (n_parts, nh, part_rows), torch.float32, dev)
     rows = part_rows if rows is None else int(rows)
+    if not 0 <= rows <= part_rows:
+        raise ValueError(f"rows must lie in [0, {part_rows}]")
     if out is None:
-        out = torch.empty((rows, nh, hd), dtype=out_dtype, device=o_partial.device)
+        out = torch.empty((rows, nh, hd), dtype=out_dtype, device=dev)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("out must be bf16 or float32")
+    _check_like(out, "out", (rows, nh, hd), out.dtype, dev)
     if lse is None:
-        lse = torch.empty((nh, rows), dtype=torch.float32, device=o_partial.device)
+        lse = torch.empty((nh, rows), dtype=torch.float32, device=dev)
         lse_head_stride = rows
+    stride = rows if lse_head_stride is None else int(lse_head_stride)
+    _check_tensor(lse, "lse")
+    if lse.dtype != torch.float32 or lse.device != dev or stride < rows or \
+            (nh > 0 and rows > 0 and lse.numel() < (nh - 1) * stride + rows):
+        raise ValueError(f"lse must be float32 on {dev} holding {nh} heads of {rows} rows at stride {stride}")
     code = _lib.ZL_BF16 if out.dtype == torch.bfloat16 else _lib.ZL_FP32
     part = _lib.ZL_BF16 if o_partial.dtype == torch.bfloat16 else _lib.ZL_FP32
-    if o_partial.dtype not in (torch.bfloat16, torch.float32):
-        raise ValueError("o_partial must be float32 or bf16")
     st = lib.zl_lse_merge_ex(_ptr(o_partial), part, _ptr(lse_partial), n_parts, rows, nh, hd, part_rows,
-                             _ptr(out), code, _ptr(lse), int(lse_head_stride or rows),
+                             _ptr(out), code, _ptr(lse), stride,
                              _stream_handle(stream))
     _lib.check(st, "zl_lse_merge_ex")
     return out, lse

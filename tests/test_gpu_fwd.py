@@ -121,6 +121,49 @@ def test_running_max_jumps(case, split):
     for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
         assert rel_l2(f64(got), ref) <= TOL_GRAD_REL_L2, (name, rel_l2(f64(got), ref))
 
+
+def test_binding_refuses_tensors_that_disagree_with_the_batch():
+    """The C ABI receives pointers only, so the binding refuses, before any
+    launch, tensors whose rows, heads, head dimension, dtype or device
+    disagree with the batch (a shorter tensor would be read or written past
+    its end)."""
+    wl = synth.Workload("chk", [100, 60], 2, 64)
+    inp = synth.make_inputs(wl, seed=0, device="cuda")
+    cu = wl.cu_seqlens()
+    q, k, v, do = inp["q"], inp["k"], inp["v"], inp["do"]
+    n0 = zl.launch_count()
+    bad_inputs = [
+        (q[:150], k, v),                          # fewer rows than cu_seqlens_q ends at
+        (q, torch.cat([k, k[:8]]), v),            # more key rows than cu_seqlens_k ends at
+        (q, k[:, :1].contiguous(), v),            # another head count
+        (q, k, v[..., :32].contiguous()),         # another head dimension
+        (q, k, v.float()),                        # another dtype
+    ]
+    for qq, kk, vv in bad_inputs:
+        with pytest.raises(ValueError):
+            zl.varlen_attn_fwd(qq, kk, vv, cu, cu)
+    with pytest.raises(ValueError):
+        zl.varlen_attn_fwd(q, k, v, cu, cu, out=torch.empty_like(q[:10]))
+    with pytest.raises(ValueError):
+        zl.varlen_attn_fwd(q, k, v, cu, cu, lse=torch.empty((2, 10), device="cuda"))
+    assert zl.launch_count() == n0
+    o, lse = zl.varlen_attn_fwd(q, k, v, cu, cu)
+    zl.sync_check()
+    n1 = zl.launch_count()
+    for args, kw in [((q, k, v, o, lse, do[:, :1].contiguous()), {}),
+                     ((q, k, v, o, lse.t().contiguous(), do), {}),
+                     ((q, k, v, o[:100], lse, do), {}),
+                     ((q, k, v, o, lse, do), {"dk": torch.empty_like(k[:100])}),
+                     ((q, k, v, o, lse, do), {"dq": torch.empty_like(q).float()})]:
+        with pytest.raises(ValueError):
+            zl.varlen_attn_bwd(*args, cu, cu, **kw)
+    part = torch.zeros((2, 16, 2, 64), device="cuda")
+    with pytest.raises(ValueError):
+        zl.lse_merge(part, torch.zeros((2, 16, 2), device="cuda"))        # [P, R, H] instead of [P, H, R]
+    with pytest.raises(ValueError):
+        zl.lse_merge(part, torch.zeros((2, 2, 16), device="cuda"), rows=17)
+    assert zl.launch_count() == n1
+
 def test_different_query_and_key_lengths():
     cu_q = [0, 5, 200, 330]
     cu_k = [0, 130, 140, 600]

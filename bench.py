@@ -507,7 +507,28 @@ def main():
         phases["merge"] = {"gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
                            "bytes_per_launch": per_launch, "avg_launch_ms": round(tot / n_l, 4)}
 
+    # ---------------- forward and fwd+bwd per configuration, each timed by itself
+    per_config = None
+    if args.per_config.strip().lower() not in ("", "none"):
+        per_config = {}
+        for n in (int(x) for x in args.per_config.split(",")):
+            per_config[str(n)] = time_config(zl, n, dev, args.seed + rank, peaks)
+
+    # ---------------- CPU oracle baseline (rank 0, single GPU)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        arrs, L, nh_s, fl = oracle_sample(wl, inp, args.oracle_tokens, args.oracle_heads)
+        secs = time_oracle(arrs, L)
+        cpu = {"value": round(fl / secs / 1e12, 5), "unit": "TFLOP/s", "cores": cpu_threads(),
+               "kind": "oracle",
+               "sample": f"float64 numpy oracle, fwd+bwd of {nh_s} heads of one {L}-token sequence of the "
+                         f"workload ({fl / 1e12:.3f} TFLOP algorithmic) in {secs:.1f} s"}
+
     # ---------------- end to end through the public API with host buffers
+    # (last: its pinned host buffers are allocated after the other legs, so a
+    # host still reclaiming memory from a process that just exited has had
+    # time to settle; copies into freshly pinned, fragmented host memory were
+    # measured several times slower right after such an exit)
     # Every step copies its four inputs in from pinned host memory and its
     # four results (O, dQ, dK, dV) back out, all inside the timed region.  The
     # copies of neighbouring steps overlap the compute of the current one
@@ -605,23 +626,6 @@ def main():
                         "tensors); the forward starts once q, k, v are in, O leaves during the backward"),
                "timeline": timeline, "clocks": e2e_clocks}
         del dev_in, dev_out, host_in, host_out, lse2
-
-    # ---------------- forward and fwd+bwd per configuration, each timed by itself
-    per_config = None
-    if args.per_config.strip().lower() not in ("", "none"):
-        per_config = {}
-        for n in (int(x) for x in args.per_config.split(",")):
-            per_config[str(n)] = time_config(zl, n, dev, args.seed + rank, peaks)
-
-    # ---------------- CPU oracle baseline (rank 0, single GPU)
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        arrs, L, nh_s, fl = oracle_sample(wl, inp, args.oracle_tokens, args.oracle_heads)
-        secs = time_oracle(arrs, L)
-        cpu = {"value": round(fl / secs / 1e12, 5), "unit": "TFLOP/s", "cores": cpu_threads(),
-               "kind": "oracle",
-               "sample": f"float64 numpy oracle, fwd+bwd of {nh_s} heads of one {L}-token sequence of the "
-                         f"workload ({fl / 1e12:.3f} TFLOP algorithmic) in {secs:.1f} s"}
 
     if world > 1:
         dist.destroy_process_group()

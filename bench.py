@@ -525,10 +525,7 @@ def main():
                          f"workload ({fl / 1e12:.3f} TFLOP algorithmic) in {secs:.1f} s"}
 
     # ---------------- end to end through the public API with host buffers
-    # (last: its pinned host buffers are allocated after the other legs, so a
-    # host still reclaiming memory from a process that just exited has had
-    # time to settle; copies into freshly pinned, fragmented host memory were
-    # measured several times slower right after such an exit)
+    # (the last leg: it pins 2 x 7.8 GB of host memory)
     # Every step copies its four inputs in from pinned host memory and its
     # four results (O, dQ, dK, dV) back out, all inside the timed region.  The
     # copies of neighbouring steps overlap the compute of the current one

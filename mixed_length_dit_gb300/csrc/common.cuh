@@ -57,12 +57,24 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
+// A kernel's translation unit may define ZL_TRY_WAIT_HINT_NS before
+// including this header: each try_wait then lets the hardware suspend the
+// waiting thread for up to that many nanoseconds (until the phase completes)
+// instead of its default time limit, so idle warps poll less.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
+#ifdef ZL_TRY_WAIT_HINT_NS
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(static_cast<uint32_t>(ZL_TRY_WAIT_HINT_NS))
+               : "memory");
+#else
   asm volatile("{\n\t.reg .pred p;\n\t"
                "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                "selp.u32 %0, 1, 0, p;\n\t}"
                : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+#endif
   return ok != 0u;
 }
 

@@ -48,20 +48,23 @@ def _last(cu) -> int:
 
 
 def _check_like(t, name, shape, dtype, device):
-    """t must be a contiguous CUDA tensor of exactly this shape, dtype and
-    device: the library receives only its pointer and writes or reads the
-    sizes that the batch implies."""
-    _check_tensor(t, name)
+    """t must have exactly this shape, dtype and device: the library receives
+    only its pointer and writes or reads the sizes that the batch implies.
+    (Whether it is a contiguous CUDA tensor is checked after every shape.)"""
     if tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != device:
         raise ValueError(f"{name} must be {tuple(shape)} {dtype} on {device}, "
                          f"got {tuple(t.shape)} {t.dtype} on {t.device}")
+
+
+def _check_cuda(**tensors):
+    for name, t in tensors.items():
+        _check_tensor(t, name)
 
 
 def _check_qkv(q, k, v, cu_seqlens_q, cu_seqlens_k):
     """q [Tq, H, d], k and v [Tk, H, d] of one dtype on one device, with Tq
     and Tk the last entries of the cu_seqlens (the packed layout of the C
     ABI), so that no tensor map or row index reaches past an allocation."""
-    _check_tensor(q, "q")
     if q.dim() != 3:
         raise ValueError("q must be [Tq, H, d]")
     tq, nh, hd = q.shape
@@ -159,6 +162,7 @@ def varlen_attn_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k=None, tiles=None, softma
         lse = torch.empty((nh, tq), dtype=torch.float32, device=q.device)
     _check_like(out, "out", q.shape, q.dtype, q.device)
     _check_like(lse, "lse", (nh, tq), torch.float32, q.device)
+    _check_cuda(q=q, k=k, v=v, out=out, lse=lse)
     if workspace is None:
         workspace = alloc_workspace(fwd_workspace_bytes(cu_seqlens_q, cu_seqlens_k, nh, hd, tiles), q.device)
     cq, nq = _lib.int32_array(cu_seqlens_q)
@@ -192,6 +196,7 @@ def varlen_attn_bwd(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k=None, tile
     _check_like(dq, "dq", q.shape, q.dtype, q.device)
     _check_like(dk, "dk", k.shape, q.dtype, q.device)
     _check_like(dv, "dv", k.shape, q.dtype, q.device)
+    _check_cuda(q=q, k=k, v=v, o=o, lse=lse, dout=dout, dq=dq, dk=dk, dv=dv)
     if workspace is None:
         workspace = alloc_workspace(bwd_workspace_bytes(cu_seqlens_q, cu_seqlens_k, nh, hd), q.device)
     cq, nq = _lib.int32_array(cu_seqlens_q)
@@ -210,7 +215,6 @@ def lse_merge(o_partial, lse_partial, rows=None, out_dtype=torch.bfloat16, out=N
     """Exact merge of partials o_partial [P, R, H, d] (float32 or bf16) /
     lse_partial [P, H, R] (float32) into (o [rows, H, d], lse [H, rows])."""
     lib = _lib.load()
-    _check_tensor(o_partial, "o_partial")
     if o_partial.dim() != 4 or o_partial.dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("o_partial must be [P, R, H, d] float32 or bf16")
     n_parts, part_rows, nh, hd = o_partial.shape
@@ -228,10 +232,10 @@ def lse_merge(o_partial, lse_partial, rows=None, out_dtype=torch.bfloat16, out=N
         lse = torch.empty((nh, rows), dtype=torch.float32, device=dev)
         lse_head_stride = rows
     stride = rows if lse_head_stride is None else int(lse_head_stride)
-    _check_tensor(lse, "lse")
     if lse.dtype != torch.float32 or lse.device != dev or stride < rows or \
             (nh > 0 and rows > 0 and lse.numel() < (nh - 1) * stride + rows):
         raise ValueError(f"lse must be float32 on {dev} holding {nh} heads of {rows} rows at stride {stride}")
+    _check_cuda(o_partial=o_partial, lse_partial=lse_partial, out=out, lse=lse)
     code = _lib.ZL_BF16 if out.dtype == torch.bfloat16 else _lib.ZL_FP32
     part = _lib.ZL_BF16 if o_partial.dtype == torch.bfloat16 else _lib.ZL_FP32
     st = lib.zl_lse_merge_ex(_ptr(o_partial), part, _ptr(lse_partial), n_parts, rows, nh, hd, part_rows,

@@ -22,6 +22,11 @@
  *   - cu_seqlens_* and tile tables are HOST arrays (int32, num_seqs + 1
  *     entries, cu[0] = 0, non-decreasing).  All other pointers are DEVICE
  *     pointers of the current CUDA device, 16-byte aligned.
+ *   - Every device buffer must hold the size the batch implies (Tq or Tk
+ *     rows of H * d elements, H * Tq LSE values, the queried workspace
+ *     bytes).  The library sees pointers, not allocations, so it cannot
+ *     check this: a shorter buffer is read or written past its end.  The
+ *     Python binding checks it against the tensors' shapes before each call.
  *   - The caller owns every buffer.  The library never calls cudaMalloc and
  *     allocates no device memory per call: scratch comes from the caller's
  *     `workspace` (zl_varlen_attn_bwd_static alone uses a fixed 64 MiB
